@@ -1,0 +1,321 @@
+"""Seeded synthetic inputs for MLA decode.
+
+This module only draws random numbers and lays them out in the byte formats
+the decode path consumes.  It holds none of the attention arithmetic, so both
+the float64 oracle (``oracle/``) and the CUDA path read the very same inputs
+without sharing any code that computes the result.
+
+Shapes follow the workloads the source pages discuss: one compressed latent KV
+row of 576 values per token (512 no-RoPE latent + 64 RoPE, FlashMLA issue #169,
+the ``D_NOPE``/``D_ROPE`` blocks of the quoted kernel), 64 or 128 query heads
+sharing it (STAGE_D2.md, "DSV4 is MQA"), 64-token pages addressed by a block
+table, and a paged slot ``page = slot // page_size`` (vLLM MlaQuery.insert).
+
+Generation order inside one workload (all from one numpy ``SeedSequence``
+with ``seed``; big arrays in seeded chunks): cache_seqlens, block_table, q, KV pool, fp8 scales, top-k.
+
+Formats (all little-endian, raw bits):
+  q            uint16 bf16 bits  [B, T, H, 576]
+  kv (bf16)    uint16 bf16 bits  [num_pages, 64, 576]
+  kv (fp8)     uint8             [num_pages, 64, 640]: bytes 0..511 are e4m3
+               no-RoPE latent, bytes 512..639 are the 64 bf16 RoPE values
+  kv_scales    float32           [num_pages, 64, 4]: one scale per 128-wide
+               tile of the no-RoPE latent; the dequantised value is
+               e4m3(byte) * scale
+  block_table  int32             [B, max_pages]
+  cache_seqlens int32            [B]
+  topk         int32             [B, T, topk] token positions within the
+               sequence, -1 for an unused slot
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+D_QK = 576
+D_V = 512
+D_ROPE = 64
+PAGE = 64
+FP8_ROW_BYTES = 640
+KV_BF16 = 0
+KV_FP8 = 1
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    q: np.ndarray                 # uint16 [B,T,H,576]
+    kv: np.ndarray                # uint16 [P,64,576] or uint8 [P,64,640]
+    kv_format: int                # KV_BF16 | KV_FP8
+    kv_scales: Optional[np.ndarray]
+    block_table: np.ndarray       # int32 [B, max_pages]
+    cache_seqlens: np.ndarray     # int32 [B]
+    topk: Optional[np.ndarray]    # int32 [B,T,k] or None
+    softmax_scale: float
+    causal: bool
+    seed: int
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.kv.shape[0])
+
+    @property
+    def topk_len(self) -> int:
+        return 0 if self.topk is None else int(self.topk.shape[2])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+_CHUNK = 1 << 24
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures
+        import os
+        _POOL = concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1))
+    return _POOL
+
+
+class _Rng:
+    """One seeded stream of draws.  Large arrays are split into fixed 16M-value
+    chunks, each with its own child seed, and drawn on a thread pool; the
+    values depend only on the seed and the order of calls."""
+
+    def __init__(self, seed: int):
+        self.ss = np.random.SeedSequence(seed)
+        self.g = np.random.Generator(np.random.PCG64(self.ss.spawn(1)[0]))
+
+    def integers(self, lo, hi, size=None):
+        return self.g.integers(lo, hi, size=size)
+
+    def permutation(self, n):
+        return self.g.permutation(n)
+
+    def uniform(self, lo, hi, size):
+        return self.g.uniform(lo, hi, size=size)
+
+    def normal_f32(self, n: int, std: float) -> np.ndarray:
+        out = np.empty(n, dtype=np.float32)
+        starts = list(range(0, n, _CHUNK))
+        kids = self.ss.spawn(len(starts))
+
+        def fill(i):
+            s = starts[i]
+            e = min(n, s + _CHUNK)
+            gi = np.random.Generator(np.random.PCG64(kids[i]))
+            gi.standard_normal(e - s, dtype=np.float32, out=out[s:e])
+            out[s:e] *= np.float32(std)
+
+        list(_pool().map(fill, range(len(starts))))
+        return out
+
+    def bytes_u8(self, n: int) -> np.ndarray:
+        out = np.empty(n, dtype=np.uint8)
+        starts = list(range(0, n, _CHUNK * 4))
+        kids = self.ss.spawn(len(starts))
+
+        def fill(i):
+            s = starts[i]
+            e = min(n, s + _CHUNK * 4)
+            gi = np.random.Generator(np.random.PCG64(kids[i]))
+            out[s:e] = gi.integers(0, 256, size=e - s, dtype=np.uint8)
+
+        list(_pool().map(fill, range(len(starts))))
+        return out
+
+
+def _round_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bits, round to nearest even (the inputs are finite)."""
+    v = x.view(np.uint32)
+    v = v + (np.uint32(0x7FFF) + ((v >> np.uint32(16)) & np.uint32(1)))
+    return (v >> np.uint32(16)).astype(np.uint16)
+
+
+def _bf16_normal(g: "_Rng", shape, std: float = 0.5) -> np.ndarray:
+    """N(0,1)*std rounded to bf16, returned as raw uint16 bits."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    starts = list(range(0, n, _CHUNK))
+    kids = g.ss.spawn(len(starts))
+
+    def fill(i):
+        s = starts[i]
+        e = min(n, s + _CHUNK)
+        gi = np.random.Generator(np.random.PCG64(kids[i]))
+        x = gi.standard_normal(e - s, dtype=np.float32)
+        x *= np.float32(std)
+        out[s:e] = _round_bf16_bits(x)
+
+    list(_pool().map(fill, range(len(starts))))
+    return out.reshape(shape)
+
+
+def _to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> OCP e4m3 bits, rounded by torch's float8_e4m3fn cast."""
+    b = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    if np.any((b & 0x7F) == 0x7F):
+        raise ValueError("e4m3 NaN code generated")
+    return b
+
+
+def make_workload(
+    name: str,
+    B: int,
+    T: int,
+    H: int,
+    seqlens: Sequence[int] | str,
+    *,
+    seed: int,
+    num_pages: Optional[int] = None,
+    identity_pages: bool = False,
+    topk: int = 0,
+    topk_pad_frac: float = 0.0,
+    topk_pad_count: Optional[int] = None,
+    fp8: bool = False,
+    causal: bool = False,
+    softmax_scale: float = 1.0 / math.sqrt(192.0),
+    seqlen_range: tuple = (1024, 32768),
+    value_std: float = 0.5,
+) -> Workload:
+    """Build one seeded workload.
+
+    seqlens: a list of B lengths, or "uniform" (each drawn from
+    ``randint(lo, hi+1)`` with ``seqlen_range = (lo, hi)``).
+    num_pages: pool size; default = the pages the sequences need.
+    identity_pages: block_table[b, j] = b * pages_per_seq + j (unpaged cache).
+    topk: indices per query token; they are distinct positions in [0, s_k[b]).
+    """
+    g = _Rng(seed)
+    if isinstance(seqlens, str):
+        assert seqlens == "uniform"
+        lo, hi = seqlen_range
+        sk = g.integers(lo, hi + 1, size=B).astype(np.int32)
+    else:
+        sk = np.asarray(seqlens, dtype=np.int32)
+        assert sk.shape == (B,)
+    pages_per = [max(1, -(-int(s) // PAGE)) for s in sk]
+    max_pages = max(pages_per)
+    need = int(sum(pages_per))
+    if num_pages is None:
+        num_pages = B * max_pages if identity_pages else need
+    assert num_pages >= need, "pool too small"
+    bt = np.full((B, max_pages), -1, dtype=np.int32)
+    if identity_pages:
+        assert num_pages >= B * max_pages
+        for b in range(B):
+            bt[b, :] = np.arange(b * max_pages, (b + 1) * max_pages, dtype=np.int32)
+    else:
+        perm = g.permutation(num_pages).astype(np.int32)
+        off = 0
+        for b in range(B):
+            bt[b, : pages_per[b]] = perm[off: off + pages_per[b]]
+            off += pages_per[b]
+    q = _bf16_normal(g, (B, T, H, D_QK), value_std)
+
+    scales = None
+    topk_arr = None
+    if topk:
+        topk_arr = np.empty((B, T, topk), dtype=np.int32)
+        n_pad = topk_pad_count if topk_pad_count is not None else int(round(topk_pad_frac * topk))
+        for b in range(B):
+            for t in range(T):
+                assert topk <= int(sk[b]), "top-k longer than the sequence"
+                idx = g.permutation(int(sk[b]))[:topk].astype(np.int32)
+                if n_pad:
+                    pos = g.permutation(topk)[:n_pad]
+                    idx[pos] = -1
+                topk_arr[b, t] = idx
+
+    if not fp8:
+        kv = _bf16_normal(g, (num_pages, PAGE, D_QK), value_std)
+        fmt = KV_BF16
+    else:
+        fmt = KV_FP8
+        kv = np.empty((num_pages, PAGE, FP8_ROW_BYTES), dtype=np.uint8)
+        scales = g.uniform(0.5, 2.0, (num_pages, PAGE, 4)).astype(np.float32)
+        if topk_arr is None:
+            # dense fp8 cache: every row drawn from the stated distribution
+            x = g.normal_f32(num_pages * PAGE * D_V, value_std).reshape(num_pages, PAGE, 4, 128)
+            kv[:, :, :D_V] = _to_e4m3_bits(x / scales[..., None]).reshape(num_pages, PAGE, D_V)
+            kv[:, :, D_V:] = _bf16_normal(g, (num_pages, PAGE, D_ROPE), value_std).view(np.uint8).reshape(num_pages, PAGE, 2 * D_ROPE)
+        else:
+            # Rows no top-k index names are never read by the method: they get
+            # random finite filler (e4m3 codes with exponent <= 14, bf16 RoPE
+            # with |v| < 2); the named rows get the stated distribution.
+            kv.reshape(-1)[:] = g.bytes_u8(kv.size)
+            kv[:, :, :D_V] &= 0x77
+            rope16 = kv[:, :, D_V:].view(np.uint16)
+            rope16 &= 0xBFFF
+            rows = set()
+            for b in range(B):
+                for t in range(T):
+                    for n in topk_arr[b, t]:
+                        if n >= 0:
+                            rows.add((b, int(n)))
+            rows = sorted(rows)
+            if rows:
+                pg = np.array([bt[b, n // PAGE] for b, n in rows], dtype=np.int64)
+                sl = np.array([n % PAGE for b, n in rows], dtype=np.int64)
+                x = g.normal_f32(len(rows) * D_V, value_std).reshape(len(rows), 4, 128)
+                kv[pg, sl, :D_V] = _to_e4m3_bits(x / scales[pg, sl][..., None]).reshape(len(rows), D_V)
+                kv[pg, sl, D_V:] = _bf16_normal(g, (len(rows), D_ROPE), value_std).view(np.uint8).reshape(len(rows), 2 * D_ROPE)
+
+    return Workload(name=name, B=B, T=T, H=H, q=q, kv=kv, kv_format=fmt,
+                    kv_scales=scales, block_table=bt, cache_seqlens=sk,
+                    topk=topk_arr, softmax_scale=float(softmax_scale),
+                    causal=bool(causal), seed=seed)
+
+
+# --- the five named workloads -------------------------------------------------
+
+CONFIG_NAMES = (
+    "tiny_dense_b2_h64_s256",
+    "paged_dense_b16_h128_s4096",
+    "varlen_split_b64_h128",
+    "sparse_fp8_b32_h64_topk2048",
+    "multitoken_causal_b32_t4_h64_s16384",
+)
+
+
+def config(i: int) -> Workload:
+    """Workload i (1-based) with seed 1000 + i."""
+    seed = 1000 + i
+    if i == 1:
+        # unpaged [2, 256, 576] cache fed as 4 pages per sequence
+        return make_workload(CONFIG_NAMES[0], 2, 1, 64, [256, 256], seed=seed,
+                             identity_pages=True, num_pages=8)
+    if i == 2:
+        return make_workload(CONFIG_NAMES[1], 16, 1, 128, [4096] * 16, seed=seed,
+                             num_pages=1024)
+    if i == 3:
+        return make_workload(CONFIG_NAMES[2], 64, 1, 128, "uniform", seed=seed,
+                             seqlen_range=(1024, 32768))
+    if i == 4:
+        return make_workload(CONFIG_NAMES[3], 32, 1, 64, [65536] * 32, seed=seed,
+                             num_pages=32768, topk=2048, topk_pad_count=102,
+                             fp8=True)
+    if i == 5:
+        return make_workload(CONFIG_NAMES[4], 32, 4, 64, [16384] * 32, seed=seed,
+                             num_pages=8192, causal=True)
+    raise ValueError(i)
+
+
+def kv_bytes_per_token(kv_format: int) -> int:
+    """Algorithmic bytes of one valid key: 576 bf16, or 512 e4m3 + 4 fp32
+    scales + 64 bf16 RoPE."""
+    return 2 * D_QK if kv_format == KV_BF16 else D_V + 16 + 2 * D_ROPE
+
+
+FLOP_PER_ROW_KEY = 2 * D_QK + 2 * D_V
