@@ -1,0 +1,431 @@
+"""MLA decode benchmark: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--config I]
+
+A step is one pass of the whole decode path over one batch: the split-KV
+metadata kernel, the decode kernel and the LSE combine kernel, on the
+variable-length workload (batch 64, one query token, 128 heads, cache
+lengths uniform in [1024, 32768], 64-token pages, bf16) unless --config picks
+another of the five named workloads.  `value` is KV-cache GB/s: the
+algorithmic bytes (1152 per valid key for bf16 rows, 656 for e4m3 + scales +
+bf16 RoPE) of the step divided by its device time, summed over ranks.
+TFLOP/s counts 2*576 + 2*512 flops per (query row, valid key).
+
+--impl reference times the float64 CPU oracle on the host cores on a
+bounded, rotating sample of the same workload (one sequence per step, all
+heads) and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MLA decode KV-cache GB/s + TFLOP/s at B=64,H=128; % of HBM/tensor roofline"
+DEFAULT_CONFIG = 3
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def valid_counts(w):
+    """Valid keys per (sequence, query token): the bench's own bookkeeping of
+    algorithmic work (dense: s_k; causal: s_k - T + t + 1; top-k: slots that
+    are not -1)."""
+    c = np.zeros((w.B, w.T), dtype=np.int64)
+    for b in range(w.B):
+        sk = int(w.cache_seqlens[b])
+        for t in range(w.T):
+            if w.topk is not None:
+                ids = w.topk[b, t]
+                c[b, t] = len(set(int(i) for i in ids if 0 <= i < sk))
+            elif w.causal:
+                c[b, t] = min(max(sk - w.T + t + 1, 0), sk)
+            else:
+                c[b, t] = sk
+    return c
+
+
+def work_of(w, batches=None):
+    """(KV bytes, flops) of the given sequences (all by default).  A key read
+    once serves every head and, for dense/causal, every query token of the
+    sequence, so KV bytes count each distinct key row once."""
+    c = valid_counts(w)
+    idx = range(w.B) if batches is None else batches
+    per_key = workloads.kv_bytes_per_token(w.kv_format)
+    kv = 0
+    fl = 0
+    for b in idx:
+        if w.topk is not None:
+            rows = set()
+            for t in range(w.T):
+                rows |= set(int(i) for i in w.topk[b, t] if 0 <= i < int(w.cache_seqlens[b]))
+            kv += len(rows) * per_key
+        else:
+            kv += int(c[b].max()) * per_key
+        fl += int(c[b].sum()) * w.H * workloads.FLOP_PER_ROW_KEY
+    return kv, fl
+
+
+class Clocks:
+    """nvidia-smi sampling (every 50 ms) around the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        if not rows:
+            return {"samples": 0}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        used = inside if inside else [min(rows, key=lambda r: abs(r[0] - (self.t0 or r[0])))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in used:
+            for n, v in zip(names, r[3][1:5]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": sorted(reasons), "samples": len(used),
+                "in_timed_region": bool(inside)}
+
+
+def traffic_record(kernel_hash: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha256") != kernel_hash:
+        return None
+    return d
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The oracle as it stands on the host cores: whole sequences (all heads)
+    in order until about budget_s seconds of work; GB/s of their KV bytes."""
+    import oracle
+    done = []
+    t0 = time.perf_counter()
+    for b in range(w.B):
+        rows = [(b, t, h) for t in range(w.T) for h in range(w.H)]
+        oracle.decode_rows(w, rows)
+        done.append(b)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    kv, fl = work_of(w, done)
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"sequences 0..{done[-1]} of {w.B} ({len(done)} x {w.T * w.H} rows, "
+                      f"{kv / 1e6:.1f} MB of KV) in {dt:.1f} s, float64",
+            "tflops": fl / dt / 1e12}
+
+
+def run_gpu(args, w, world, rank, local):
+    import torch
+    import mla_decode_attention_05_gb300 as mla
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    q_h = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
+    if w.kv_format == workloads.KV_BF16:
+        kv_h = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16)
+        sc_h = None
+    else:
+        kv_h = torch.from_numpy(w.kv)
+        sc_h = torch.from_numpy(w.kv_scales)
+    bt_h = torch.from_numpy(w.block_table)
+    sk_h = torch.from_numpy(w.cache_seqlens)
+    tk_h = None if w.topk is None else torch.from_numpy(w.topk)
+    host = [x for x in (q_h, kv_h, sc_h, bt_h, sk_h, tk_h) if x is not None]
+    q, kv, bt, sk = (x.to(dev) for x in (q_h, kv_h, bt_h, sk_h))
+    sc = None if sc_h is None else sc_h.to(dev)
+    tk = None if tk_h is None else tk_h.to(dev)
+    parts = mla.default_num_parts(dev)
+    topk = w.topk_len
+    ws = torch.empty(mla.workspace_bytes(w.B, w.H, w.T, topk, parts), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    md = torch.empty((parts, 8), dtype=torch.int32, device=dev)
+    nitems = mla.num_items(w.B, w.H, w.T, topk)
+    ns = torch.empty(nitems + 1, dtype=torch.int32, device=dev)
+    L = mla.lib()
+    import ctypes
+    P = ctypes.c_void_p
+    sptr = P(stream.cuda_stream)
+
+    def step(qq, kk, bb, ss, ss_sc, tt, oo, ll):
+        rc = L.mla_decode_metadata(P(ss.data_ptr()), w.B, w.H, w.T, topk, int(w.causal), parts,
+                                   P(md.data_ptr()), P(ns.data_ptr()), sptr)
+        if rc != 0:
+            raise RuntimeError(L.mla_last_error_string().decode())
+        rc = L.mla_decode(P(qq.data_ptr()), P(kk.data_ptr()), w.kv_format, w.num_pages, 64,
+                          P(bb.data_ptr()), w.max_pages, P(ss.data_ptr()),
+                          None if tt is None else P(tt.data_ptr()), topk, None,
+                          None if ss_sc is None else P(ss_sc.data_ptr()),
+                          ctypes.c_float(w.softmax_scale), int(w.causal), P(md.data_ptr()),
+                          P(ns.data_ptr()), parts, P(ws.data_ptr()), ws.numel(),
+                          P(oo.data_ptr()), P(ll.data_ptr()), w.B, w.T, w.H, sptr)
+        if rc != 0:
+            raise RuntimeError(L.mla_last_error_string().decode())
+
+    launches_per_step = 3  # metadata, decode, combine
+    for _ in range(args.warmup):
+        step(q, kv, bt, sk, sc, tk, out, lse)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_b + ev_a:   # create the underlying events before handing them over
+        e.record(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
+    start.record(stream)
+    for i in range(K):
+        mla.profile_events(ev_b[i], ev_a[i])
+        step(q, kv, bt, sk, sc, tk, out, lse)
+    end.record(stream)
+    mla.profile_events()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    kern_ms = [b.elapsed_time(a) for b, a in zip(ev_b, ev_a)]
+    status = mla.device_status()
+    clk = clocks.finish() if clocks else None
+
+    # end to end through the C ABI with host buffers: pinned host -> device
+    # copies of every input, the three kernels, device -> host of out + lse
+    pinned = [x.pin_memory() for x in host]
+    dev_bufs = [torch.empty_like(x, device=dev) for x in host]
+    o_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    l_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    names = [n for n, x in zip(("q", "kv", "sc", "bt", "sk", "tk"), (q_h, kv_h, sc_h, bt_h, sk_h, tk_h)) if x is not None]
+    D = dict(zip(names, dev_bufs))
+
+    def e2e_step():
+        for hb, db in zip(pinned, dev_bufs):
+            db.copy_(hb, non_blocking=True)
+        step(D["q"], D["kv"], D["bt"], D["sk"], D.get("sc"), D.get("tk"), out, lse)
+        o_h.copy_(out, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+
+    Ke = max(3, min(K, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2) / Ke
+    return dict(total_ms=total_ms, kern_ms=kern_ms, status=status, clocks=clk, parts=parts,
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, launches=launches_per_step * K)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args.gpus)
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workloads.config(args.config)
+        import oracle
+        order = list(range(w.B))
+        per = []
+        done_kv = 0
+        for i in range(args.warmup + args.steps):
+            b = order[i % w.B]
+            rows = [(b, t, h) for t in range(w.T) for h in range(w.H)]
+            t0 = time.perf_counter()
+            oracle.decode_rows(w, rows)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                kvb, _ = work_of(w, [b])
+                per.append((dt, kvb))
+        tot_t = sum(p[0] for p in per)
+        tot_kv = sum(p[1] for p in per)
+        val = tot_kv / tot_t / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(per),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H},
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                                 "sample": f"one sequence (all {w.T * w.H} query rows) per step, rotating over the {w.B} sequences"},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    w = workloads.config(args.config)
+    kv_bytes, flops = work_of(w)
+    r = run_gpu(args, w, world, rank, local)
+    step_ms = max_over_ranks(r["total_ms"] / args.steps, world)
+    kern_ms = statistics.mean(r["kern_ms"])
+    kern_ms_max = max_over_ranks(kern_ms, world)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    if rank != 0:
+        return
+    gbs = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    tflops = world * flops / (step_ms * 1e-3) / 1e12
+    roof_us = max(kv_bytes / (hbm * 1e9), flops / (tf_burst * 1e12)) * 1e6
+    bound = "hbm" if kv_bytes / hbm >= flops / (tf_burst * 1e3) else "tensor"
+    k_gbs = kv_bytes / (kern_ms_max * 1e-3) / 1e9
+    k_tf = flops / (kern_ms_max * 1e-3) / 1e12
+    tr = traffic_record(kernel_source_hash())
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": k_gbs, "peak": hbm, "unit": "GB/s", "frac": k_gbs / hbm,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src}
+    else:
+        roof = {"bound": "tensor", "achieved": k_tf, "peak": tf_burst, "unit": "TFLOP/s", "frac": k_tf / tf_burst,
+                "peak_source": f"{peak_src} bf16 burst"}
+    roof["traffic"] = None if tr is None else tr["dram_bytes_per_launch"]
+    roof["kernel_ms"] = kern_ms_max
+    roof["tflops"] = k_tf
+    roof["frac_of_roofline_time"] = (roof_us * 1e-3) / kern_ms_max
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tflops": tflops, "roofline_time_us": roof_us, "frac_of_roofline": (roof_us * 1e-3) / step_ms,
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "kv_format": "bf16" if w.kv_format == 0 else "fp8_e4m3",
+                   "causal": w.causal, "topk": w.topk_len, "page_size": 64, "num_parts": r["parts"],
+                   "kv_bytes": kv_bytes, "flops": flops, "seed": w.seed,
+                   "l2": f"inputs larger than L2 ({w.kv.nbytes / 1e9:.2f} GB cache vs {L2_BYTES / 1e6:.0f} MB L2); no flush",
+                   "parallelism": f"weak, {world} independent replica(s)"},
+        "roofline": roof,
+        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "device_status": r["status"],
+        "clocks": r["clocks"],
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * Multi-head latent attention decode: every query head of a sequence attends
+ * to one shared latent KV row per cached token (STAGE_D2.md, "DSV4 is MQA":
+ * Q is per head, K/V has a single head shared by all query heads).  A row
+ * holds 576 values, a 512-wide no-RoPE latent followed by 64 RoPE values; the
+ * RoPE part is simply one more block of the QK reduction and V is the first
+ * 512 values (FlashMLA issue #169 "dual gemm": RoPE behaves like an extra
+ * block of size 64; the D_ROPE / D_NOPE split of the quoted kernel).  For
+ * query row (b, t, h):
+ *
+ *   s_n = softmax_scale * sum_{d<576} q[b,t,h,d] * K_n[d]      n in N(b,t)
+ *   lse = ln sum_n exp(s_n)                  (natural log; -inf if N empty)
+ *   out = sum_n exp(s_n - lse) * K_n[0:512]  (0 if N empty)
+ *
+ * where N(b,t) = {n < s_k}                       dense
+ *               {n < s_k - T + t + 1}           causal (query token t of T)
+ *               {topk[b,t,j] : j, != -1}        sparse top-k
+ * and K_n is the cache row of logical token n of sequence b, found at page
+ * block_table[b][n / 64], slot n % 64 (vLLM MlaQuery.insert: page, offset =
+ * slot // page_size, slot % page_size).
+ *
+ * Ownership: the caller owns every buffer; the library allocates no device or
+ * host memory of its own on these paths (a small host-side cache of TMA
+ * descriptors aside).  Every call is asynchronous on `stream` and never
+ * synchronises the host, except mla_device_status().
+ *
+ * Errors: each call returns MLA_OK (0) or a negative code; the text of the
+ * last error of the calling thread is kept for mla_last_error_string().
+ * Argument checks happen on the host before anything is launched: a call that
+ * returns an error has enqueued nothing.  Values that only the device can see
+ * (a page id outside the pool, a top-k index at or beyond s_k, a negative
+ * s_k) never fault or trap: the row is skipped (treated as -1 / length 0) and
+ * a bit is set in a device status word that mla_device_status() reads.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or flag */
+#define MLA_ERR_UNSUPPORTED (-2) /* valid request this build does not serve   */
+#define MLA_ERR_WORKSPACE (-3)   /* workspace null or smaller than required   */
+#define MLA_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed         */
+
+#define MLA_KV_BF16 0     /* row = 576 bf16 (1152 bytes)                        */
+#define MLA_KV_FP8_E4M3 1 /* row = 512 e4m3 bytes + 64 bf16 RoPE (640 bytes),
+                             plus 4 fp32 scales per row in kv_scales            */
+
+/* Device status bits (mla_device_status). */
+#define MLA_STATUS_BAD_PAGE 1u      /* block_table entry outside [0, num_pages) */
+#define MLA_STATUS_BAD_TOPK 2u      /* top-k index >= s_k or < -1               */
+#define MLA_STATUS_BAD_SEQLEN 4u    /* negative s_k, or more pages than max_pages */
+#define MLA_STATUS_WAIT_TIMEOUT 8u  /* a bounded device wait gave up            */
+
+/* Limits of this build. */
+#define MLA_PAGE_SIZE 64
+#define MLA_MAX_HEADS 128
+#define MLA_MAX_QUERY_TOKENS 16
+#define MLA_MAX_ITEMS 8192 /* work items = B * ceil(T*H/128), or B*T with top-k */
+
+/* cudaStream_t-compatible handle (a CUstream). NULL = the legacy stream. */
+typedef struct CUstream_st *mla_stream_t;
+
+/*
+ * Number of workers the split-KV partition should target on `device`: the
+ * decode kernel runs one persistent cluster of two CTAs per worker, so this
+ * is the SM count / 2 (76 on a 152-SM GB300).  Returns <= 0 on error.
+ */
+int mla_default_num_parts(int device);
+
+/* Work items of a request (see mla_decode_metadata), or a negative code. */
+int mla_decode_num_items(int B, int H, int T, int topk);
+
+/*
+ * Element counts of the two metadata arrays for a request:
+ *   tile_md     int32 [num_parts][8]
+ *   num_splits  int32 [num_items + 1]
+ */
+int mla_decode_metadata_sizes(int B, int H, int T, int topk, int num_parts,
+                              size_t *tile_md_elems, size_t *num_splits_elems);
+
+/*
+ * Split-KV scheduling (STAGE_D2.md, "Grid vs. Persistent Tile Scheduler": a
+ * persistent scheduler balances variable sequence lengths over a fixed set
+ * of workers).  One small device kernel on `stream` reads cache_seqlens and
+ * writes the partition of all key tiles over num_parts workers.
+ *
+ *   cache_seqlens  device int32 [B]            s_k per sequence (>= 0)
+ *   B, H, T        batch, query heads (1..128), query tokens (1..16)
+ *   topk           0 = dense/causal; > 0 = top-k length (keys per query token)
+ *   causal         0/1; must be 0 when topk > 0
+ *   num_parts      workers (>= 1); pass mla_default_num_parts(device)
+ *   tile_md        device int32 [num_parts][8], written
+ *   num_splits     device int32 [num_items + 1], written
+ *
+ * Rule (identical on host and device; one 64-key tile per cache page):
+ * items are M tiles of up to 128 query rows (row = t*H + h) per sequence, or
+ * one query token per item with top-k; item i has n_i key tiles (ceil(s_k/64);
+ * causal: ceil(min(s_k, s_k - T + t_last + 1)/64); top-k: ceil(topk/64)) and
+ * costs n_i + 4 on a line; the line is cut into num_parts equal segments of
+ * L = ceil(total / num_parts) and each tile belongs to the segment holding
+ * its coordinate.  tile_md[p] = {begin_item, begin_tile, last_item,
+ * end_tile (exclusive), first_piece, begin_at_item_start, 0, 0}; num_splits
+ * is the exclusive prefix over items of the number of workers per item.
+ * The arrays are only meaningful to mla_decode with the same B, H, T, topk,
+ * causal, num_parts and cache_seqlens.
+ */
+int mla_decode_metadata(const int32_t *cache_seqlens, int B, int H, int T,
+                        int topk, int causal, int num_parts, int32_t *tile_md,
+                        int32_t *num_splits, mla_stream_t stream);
+
+/*
+ * Bytes of workspace mla_decode needs: fp32 partial outputs and partial LSEs
+ * of the split items, (num_items + num_parts) x 128 rows x (512 + 1) floats,
+ * rounded up to 256 bytes.
+ */
+size_t mla_decode_workspace_bytes(int B, int H, int T, int topk, int num_parts);
+
+/*
+ * MLA decode attention (the formula at the top of this file).
+ *
+ *   q              device bf16 [B][T][H][576]   (row-major, 16-byte aligned)
+ *   kv_cache       device, MLA_KV_BF16: bf16 [num_pages][64][576];
+ *                  MLA_KV_FP8_E4M3: bytes [num_pages][64][640] (16-byte aligned)
+ *   kv_format      MLA_KV_BF16 or MLA_KV_FP8_E4M3
+ *   num_pages      pages in the pool; page_size must be 64
+ *   block_table    device int32 [B][max_pages]: page of the j-th 64 tokens
+ *   cache_seqlens  device int32 [B]: s_k per sequence
+ *   topk_indices   device int32 [B][T][topk] or NULL: token positions within
+ *                  the sequence, -1 = unused slot; requires causal == 0
+ *   gathered       device int32 [B][T][topk] or NULL (top-k only): if given,
+ *                  the kernel writes, per slot, the token position whose row
+ *                  it loaded, or -1 for a slot it skipped
+ *   kv_scales      device fp32 [num_pages][64][4] for MLA_KV_FP8_E4M3
+ *                  (value = e4m3(byte) * kv_scales[page][slot][d / 128]),
+ *                  else NULL
+ *   softmax_scale  > 0 (1/sqrt(192) for the 128 no-PE + 64 RoPE query dims)
+ *   causal         0/1
+ *   tile_md, num_splits, num_parts   from mla_decode_metadata
+ *   workspace      device, >= mla_decode_workspace_bytes(...), 256-aligned
+ *   out            device bf16 [B][T][H][512], written
+ *   lse            device fp32 [B][H][T], written (natural log)
+ *
+ * Launches the decode kernel and, when some item was split over several
+ * workers, the LSE combine kernel, both on `stream`.  Cache rows past s_k in
+ * a sequence's last page are read but carry zero weight; they must hold
+ * finite values (a NaN there would reach `out` through 0 * NaN).
+ */
+int mla_decode(const void *q, const void *kv_cache, int kv_format,
+               int num_pages, int page_size, const int32_t *block_table,
+               int max_pages, const int32_t *cache_seqlens,
+               const int32_t *topk_indices, int topk, int32_t *gathered,
+               const float *kv_scales, float softmax_scale, int causal,
+               const int32_t *tile_md, const int32_t *num_splits,
+               int num_parts, void *workspace, size_t workspace_bytes,
+               void *out, float *lse, int B, int T, int H,
+               mla_stream_t stream);
+
+/* Text of the calling thread's last error ("" if none). */
+const char *mla_last_error_string(void);
+
+/*
+ * Reads and clears the device status word of the current device (an OR of
+ * MLA_STATUS_* bits set by earlier kernels).  Synchronous: waits for all
+ * work on the device.  Returns MLA_OK or MLA_ERR_CUDA.
+ */
+int mla_device_status(uint32_t *status);
+
+/*
+ * Profiling hook: when both are non-NULL cudaEvent_t handles, every later
+ * mla_decode call on this thread records `before` on its stream right before
+ * the decode kernel launch and `after` right after it (the combine kernel
+ * is outside).  Pass NULL, NULL to stop.  Returns MLA_OK.
+ */
+int mla_profile_events(void *before, void *after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,219 @@
+"""MLA decode attention for GB300 (sm_103a): Python binding.
+
+Argument marshalling over the C ABI of ``_lib/libmla_decode.so`` (declared in
+``include/mla_decode.h``).  Every step of the computation runs in the
+library's CUDA kernels; PyTorch only provides device memory (outputs and
+workspace are ``torch.empty``) and the current CUDA stream.  There is no CPU
+path: if the library has not been built, importing the binding works but
+every call raises.
+
+    import mla_decode_attention_05_gb300 as mla
+    tile_md, num_splits = mla.metadata(cache_seqlens, H, T)
+    out, lse = mla.decode(q, kv_cache, block_table, cache_seqlens,
+                          softmax_scale=192 ** -0.5,
+                          tile_md=tile_md, num_splits=num_splits)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmla_decode.so")
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+PAGE_SIZE = 64
+D_QK = 576
+D_V = 512
+FP8_ROW_BYTES = 640
+STATUS_BAD_PAGE = 1
+STATUS_BAD_TOPK = 2
+STATUS_BAD_SEQLEN = 4
+STATUS_WAIT_TIMEOUT = 8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"mla error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """The loaded C library (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                    "or python -m mla_decode_attention_05_gb300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.mla_default_num_parts.argtypes = [i]
+            L.mla_decode_num_items.argtypes = [i, i, i, i]
+            L.mla_decode_metadata_sizes.argtypes = [i, i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            L.mla_decode_metadata.argtypes = [P, i, i, i, i, i, i, P, P, P]
+            L.mla_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+            L.mla_decode_workspace_bytes.restype = sz
+            L.mla_decode.argtypes = [P, P, i, i, i, P, i, P, P, i, P, P, ctypes.c_float, i,
+                                     P, P, i, P, sz, P, P, i, i, i, P]
+            L.mla_last_error_string.restype = ctypes.c_char_p
+            L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.mla_profile_events.argtypes = [P, P]
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc < 0:
+        raise MlaError(rc, lib().mla_last_error_string().decode())
+    return rc
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def default_num_parts(device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
+    return _check(lib().mla_default_num_parts(dev.index))
+
+
+def num_items(B: int, H: int, T: int, topk: int = 0) -> int:
+    return _check(lib().mla_decode_num_items(B, H, T, topk))
+
+
+def workspace_bytes(B: int, H: int, T: int, topk: int, num_parts: int) -> int:
+    n = lib().mla_decode_workspace_bytes(B, H, T, topk, num_parts)
+    if n == 0:
+        raise MlaError(-1, "bad sizes for workspace query")
+    return int(n)
+
+
+def metadata(cache_seqlens: torch.Tensor, H: int, T: int, *, topk: int = 0,
+             causal: bool = False, num_parts: Optional[int] = None):
+    """Split-KV schedule on the current stream -> (tile_md, num_splits)."""
+    _need(cache_seqlens, "cache_seqlens", torch.int32, ndim=1)
+    dev = cache_seqlens.device
+    B = cache_seqlens.shape[0]
+    if num_parts is None:
+        num_parts = default_num_parts(dev)
+    a = ctypes.c_size_t()
+    b = ctypes.c_size_t()
+    _check(lib().mla_decode_metadata_sizes(B, H, T, topk, num_parts, ctypes.byref(a), ctypes.byref(b)))
+    tile_md = torch.empty(a.value, dtype=torch.int32, device=dev).view(num_parts, 8)
+    num_splits = torch.empty(b.value, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().mla_decode_metadata(_ptr(cache_seqlens), B, H, T, topk, int(bool(causal)),
+                                         num_parts, _ptr(tile_md), _ptr(num_splits), _stream(dev)))
+    return tile_md, num_splits
+
+
+def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+           cache_seqlens: torch.Tensor, *, softmax_scale: float,
+           causal: bool = False, topk_indices: Optional[torch.Tensor] = None,
+           kv_scales: Optional[torch.Tensor] = None,
+           tile_md: Optional[torch.Tensor] = None,
+           num_splits: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+           gathered: Optional[torch.Tensor] = None):
+    """MLA decode on the current stream -> (out bf16 [B,T,H,512], lse fp32 [B,H,T]).
+
+    q bf16 [B,T,H,576]; kv_cache bf16 [P,64,576] (bf16 rows) or uint8
+    [P,64,640] (e4m3 latent + bf16 RoPE rows, with kv_scales fp32 [P,64,4]);
+    block_table int32 [B,max_pages]; cache_seqlens int32 [B]; topk_indices
+    int32 [B,T,topk] or None.  tile_md/num_splits come from metadata() with
+    the same arguments (computed here when omitted)."""
+    _need(q, "q", torch.bfloat16, ndim=4)
+    dev = q.device
+    B, T, H, dq = q.shape
+    if dq != D_QK:
+        raise ValueError("q must be [B, T, H, 576]")
+    if kv_cache.dtype == torch.bfloat16:
+        fmt = KV_BF16
+        if kv_cache.dim() != 3 or kv_cache.shape[2] != D_QK:
+            raise ValueError("bf16 kv_cache must be [P, 64, 576]")
+    elif kv_cache.dtype == torch.uint8:
+        fmt = KV_FP8_E4M3
+        if kv_cache.dim() != 3 or kv_cache.shape[2] != FP8_ROW_BYTES:
+            raise ValueError("fp8 kv_cache must be uint8 [P, 64, 640]")
+        _need(kv_scales, "kv_scales", torch.float32, dev, 3)
+    else:
+        raise TypeError("kv_cache must be bfloat16 or uint8 (fp8 rows)")
+    _need(kv_cache, "kv_cache", kv_cache.dtype, dev)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev, 1)
+    if block_table.shape[0] != B or cache_seqlens.shape[0] != B:
+        raise ValueError("block_table / cache_seqlens batch mismatch")
+    topk = 0
+    if topk_indices is not None:
+        _need(topk_indices, "topk_indices", torch.int32, dev, 3)
+        if tuple(topk_indices.shape[:2]) != (B, T):
+            raise ValueError("topk_indices must be [B, T, topk]")
+        topk = topk_indices.shape[2]
+    if gathered is not None:
+        _need(gathered, "gathered", torch.int32, dev, 3)
+    if tile_md is None or num_splits is None:
+        tile_md, num_splits = metadata(cache_seqlens, H, T, topk=topk, causal=causal)
+    num_parts = tile_md.shape[0]
+    need = workspace_bytes(B, H, T, topk, num_parts)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, 4)
+    _need(lse, "lse", torch.float32, dev, 3)
+    with torch.cuda.device(dev):
+        _check(lib().mla_decode(
+            _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1],
+            _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+            _ptr(topk_indices), topk, _ptr(gathered), _ptr(kv_scales),
+            float(softmax_scale), int(bool(causal)), _ptr(tile_md), _ptr(num_splits),
+            num_parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
+    return out, lse
+
+
+def device_status() -> int:
+    """Read and clear the device status word (synchronises the device)."""
+    v = ctypes.c_uint32()
+    _check(lib().mla_device_status(ctypes.byref(v)))
+    return int(v.value)
+
+
+def profile_events(before=None, after=None):
+    """Record CUDA events around the decode kernel of later decode() calls on
+    this thread (torch.cuda.Event objects), or stop with no arguments."""
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else None
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else None
+    _check(lib().mla_profile_events(b, a))

@@ -1,0 +1,85 @@
+"""The C ABI: the library builds, loads without a GPU and exports every entry
+point that include/*.h declares; host-side argument checks reject bad calls
+before anything is launched (no compute call is made here)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mla_decode_attention_05_gb300 import build
+    build.build()
+    import mla_decode_attention_05_gb300 as m
+    return m.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(mla_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"mla_decode", "mla_decode_metadata", "mla_decode_workspace_bytes"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_sizes_and_items(L):
+    import mla_decode_attention_05_gb300 as m
+    assert m.num_items(64, 128, 1) == 64
+    assert m.num_items(32, 64, 4) == 64          # T*H = 256 rows -> 2 M tiles
+    assert m.num_items(32, 64, 1, topk=2048) == 32
+    assert m.num_items(2, 64, 3, topk=10) == 6   # top-k: one item per query token
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.mla_decode_metadata_sizes(16, 128, 1, 0, 76, ctypes.byref(a), ctypes.byref(b)) == 0
+    assert (a.value, b.value) == (76 * 8, 17)
+    ws = m.workspace_bytes(64, 128, 1, 0, 76)
+    assert ws % 256 == 0 and ws >= (64 + 76) * 128 * 513 * 4
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(B=0), -1), (dict(H=129), -1), (dict(T=17), -1), (dict(page_size=32), -2),
+    (dict(kv_format=7), -1), (dict(softmax_scale=0.0), -1), (dict(causal=1, topk=8), -1),
+    (dict(workspace_bytes=16), -3), (dict(num_parts=0), -1), (dict(q=0), -1),
+    (dict(q=8), -1),
+])
+def test_argument_checks(L, args, code):
+    """Each bad argument returns its error code and an explanation; the
+    checks run before any CUDA call, so this needs no device."""
+    base = dict(q=256, kv=256, kv_format=0, num_pages=4, page_size=64, bt=256, max_pages=4,
+                sk=256, topk_ptr=None, topk=0, gathered=None, scales=None,
+                softmax_scale=0.07, causal=0, md=256, ns=256, num_parts=4, ws=256,
+                workspace_bytes=1 << 30, out=256, lse=256, B=2, T=1, H=64)
+    base.update(args)
+    if base["topk"] and base["topk_ptr"] is None:
+        base["topk_ptr"] = 256
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = L.mla_decode(v(base["q"]), v(base["kv"]), base["kv_format"], base["num_pages"],
+                      base["page_size"], v(base["bt"]), base["max_pages"], v(base["sk"]),
+                      v(base["topk_ptr"]), base["topk"], v(base["gathered"]), v(base["scales"]),
+                      ctypes.c_float(base["softmax_scale"]), base["causal"], v(base["md"]),
+                      v(base["ns"]), base["num_parts"], v(base["ws"]), base["workspace_bytes"],
+                      v(base["out"]), v(base["lse"]), base["B"], base["T"], base["H"], None)
+    assert rc == code
+    assert len(L.mla_last_error_string()) > 0
+
+
+def test_library_missing_fails_loudly(tmp_path, monkeypatch):
+    """No silent fallback: without the built library every call raises."""
+    import mla_decode_attention_05_gb300 as m
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError):
+        m.num_items(1, 64, 1)
