@@ -172,6 +172,15 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def subset(w, nb: int):
+    """The first nb sequences of a workload (the page pool is kept whole)."""
+    import dataclasses
+    nb = min(nb, w.B)
+    return dataclasses.replace(
+        w, name=f"{w.name}[:{nb}]", B=nb, q=w.q[:nb].copy(), block_table=w.block_table[:nb].copy(),
+        cache_seqlens=w.cache_seqlens[:nb].copy(), topk=None if w.topk is None else w.topk[:nb].copy())
+
+
 def dist_setup(gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -343,6 +352,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first BATCH sequences of the workload (same values; "
+                         "used for small profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
@@ -380,6 +392,8 @@ def main():
         return
 
     w = workloads.config(args.config)
+    if args.batch:
+        w = subset(w, args.batch)
     kv_bytes, flops = work_of(w)
     r = run_gpu(args, w, world, rank, local)
     step_ms = max_over_ranks(r["total_ms"] / args.steps, world)

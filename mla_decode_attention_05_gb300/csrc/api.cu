@@ -74,7 +74,7 @@ int check_shape(int B, int H, int T, int topk) {
 int items_of(int B, int H, int T, int topk) { return topk > 0 ? B * T : B * n_mt_of(H, T); }
 
 struct WsLayout {
-  size_t lse_off, o_off, total;
+  size_t lse_off, o_off, p_off, total;
 };
 
 WsLayout ws_layout(int n_items, int num_parts) {
@@ -84,7 +84,9 @@ WsLayout ws_layout(int n_items, int num_parts) {
   size_t lse_bytes = slots * mla::M_TILE * sizeof(float);
   l.o_off = (lse_bytes + 255) / 256 * 256;
   size_t o_bytes = slots * mla::M_TILE * mla::D_V * sizeof(float);
-  l.total = (l.o_off + o_bytes + 255) / 256 * 256;
+  l.p_off = (l.o_off + o_bytes + 255) / 256 * 256;
+  size_t p_bytes = (size_t)num_parts * mla::P_RING * mla::P_SLOT_BYTES;
+  l.total = (l.p_off + p_bytes + 255) / 256 * 256;
   return l;
 }
 
@@ -197,6 +199,7 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   p.num_splits = num_splits;
   p.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + wl.lse_off);
   p.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + wl.o_off);
+  p.ws_p = static_cast<uint8_t *>(workspace) + wl.p_off;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.lse = lse;
   p.status = st;

@@ -17,6 +17,10 @@ constexpr int M_TILE = 128;  // query rows per work item
 constexpr int FIXED_COST = 4;
 constexpr int MD_STRIDE = 8; // ints per tile_md entry
 constexpr int FP8_ROW = 640; // 512 e4m3 + 64 bf16 RoPE bytes
+// P messages from the S engine to the O engine of a worker pass through a
+// small ring in the workspace (L2-resident): P_RING slots of P_SLOT_BYTES.
+constexpr int P_RING = 4;
+constexpr int P_SLOT_BYTES = 17920;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -33,6 +37,7 @@ struct DecodeParams {
   const int32_t *num_splits;
   float *ws_lse;  // [slots][128] (log2 domain)
   float *ws_o;    // [slots][128][512]
+  uint8_t *ws_p;  // [num_parts][P_RING][P_SLOT_BYTES]
   __nv_bfloat16 *out;
   float *lse;
   unsigned int *status;
