@@ -74,7 +74,7 @@ constexpr uint32_t OFF_LPART = kStages0 * kStage0Bytes;            // rank 0: fl
 
 // TMEM columns
 constexpr uint32_t TM_Q = 0;      // rank 0: 288 columns (576 bf16 per row)
-constexpr uint32_t TM_S = 288;    // rank 0: two S buffers of 64 columns
+constexpr uint32_t TM_S = 320;    // rank 0: two S buffers of 64 columns (64-aligned)
 constexpr uint32_t TM_O = 0;      // rank 1: 512 columns
 constexpr uint32_t TM_COLS = 512;
 
@@ -379,13 +379,16 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
       if (!wait_or_abort(c, &br.kv_full[s], (g / kStages0) & 1)) return false;
       if (!wait_or_abort(c, &br.s_free[b], (u & 1) ^ 1)) return false;
       tc_fence_after();
-      const uint32_t kvs = kv0 + s * kStage0Bytes;
-      for (int kb = 0; kb < 9; kb++) {
+      // One base descriptor per tile; block kb / step kk only move its
+      // start-address field (16-byte units: 512 per 8 KB block, 2 per 32 B),
+      // which stays below 2^14 for every address of the shared map.
+      const uint64_t kd0 = smem_desc_sw128(kv0 + s * kStage0Bytes, 16, 1024);
+      const uint32_t d = tmem + TM_S + b * 64;
+      mma_ts(d, tmem + TM_Q, kd0, IDESC_QK, 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          const uint64_t kd = smem_desc_sw128(kvs + kb * kBlkBytes + kk * 32, 16, 1024);
-          mma_ts(tmem + TM_S + b * 64, tmem + TM_Q + kb * 32 + kk * 8, kd, IDESC_QK, (kb | kk) != 0 ? 1u : 0u);
-        }
+      for (int i = 1; i < 36; i++) {
+        const int kb = i >> 2, kk = i & 3;
+        mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, 1u);
       }
       mma_commit(smem_u32(&br.s_full[b]));
       mma_commit(smem_u32(&br.kv_empty[s]));
