@@ -167,6 +167,50 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
                void *out, float *lse, int B, int T, int H,
                mla_stream_t stream);
 
+/*
+ * Size of the fixed device scratch of mla_decode_noalloc (64 MiB per device).
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * MLA decode for callers that cannot allocate device memory.  (No counterpart
+ * on the source pages: this is a convenience of this library.)
+ *
+ * Some callers cannot provide the schedule arrays and the workspace that
+ * mla_decode_metadata / mla_decode take: the host program may own every byte
+ * of device memory (a runtime that plans all of its memory up front, or a
+ * plugin contract that forbids the plugin from allocating), or the call may
+ * come through a foreign-function layer with no device allocator at hand.
+ * This entry point takes the same inputs and outputs as mla_decode (no
+ * `gathered` record) and keeps its scratch in one array of
+ * MLA_NOALLOC_SCRATCH_BYTES inside the library's device memory, which every
+ * GPU that loads the library holds until the process exits.  It runs the same
+ * metadata, decode and combine kernels, with mla_default_num_parts(device)
+ * workers, and allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library call.
+ *
+ *   Limits: requests whose schedule + workspace would exceed the scratch (on a
+ *   152-SM GB300 that is more than about 160 work items, e.g. B > ~160 for
+ *   T = 1, H = 128) return MLA_ERR_WORKSPACE, with the byte counts in
+ *   mla_last_error_string(); use mla_decode for those.
+ *   Set-up: the first call on a device, with that device current, looks up
+ *   the scratch's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.
+ *   Sharing: all calls on a device share the one scratch, which keeps the last
+ *   call's contents (nothing in it needs to start at zero).  Calls whose
+ *   kernels overlap on the GPU (different streams, or threads without
+ *   ordering) race on it; issue them in order on one stream.
+ *   Errors: as mla_decode; an argument error is reported before anything is
+ *   enqueued.
+ */
+int mla_decode_noalloc(const void *q, const void *kv_cache, int kv_format,
+                       int num_pages, int page_size, const int32_t *block_table,
+                       int max_pages, const int32_t *cache_seqlens,
+                       const int32_t *topk_indices, int topk,
+                       const float *kv_scales, float softmax_scale, int causal,
+                       void *out, float *lse, int B, int T, int H,
+                       mla_stream_t stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *mla_last_error_string(void);
 

@@ -65,6 +65,8 @@ def lib():
             L.mla_decode_workspace_bytes.restype = sz
             L.mla_decode.argtypes = [P, P, i, i, i, P, i, P, P, i, P, P, ctypes.c_float, i,
                                      P, P, i, P, sz, P, P, i, i, i, P]
+            L.mla_decode_noalloc.argtypes = [P, P, i, i, i, P, i, P, P, i, P, ctypes.c_float, i,
+                                             P, P, i, i, i, P]
             L.mla_last_error_string.restype = ctypes.c_char_p
             L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.mla_profile_events.argtypes = [P, P]
@@ -201,6 +203,31 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
             float(softmax_scale), int(bool(causal)), _ptr(tile_md), _ptr(num_splits),
             num_parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
             _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
+    return out, lse
+
+
+def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                   cache_seqlens: torch.Tensor, *, softmax_scale: float, causal: bool = False,
+                   topk_indices: Optional[torch.Tensor] = None,
+                   kv_scales: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """decode() for callers that cannot allocate device memory: schedule and
+    workspace live in the library's fixed device scratch (mla_decode_noalloc).
+    Only out / lse are created here when not given."""
+    _need(q, "q", torch.bfloat16, ndim=4)
+    dev = q.device
+    B, T, H, _ = q.shape
+    fmt = KV_BF16 if kv_cache.dtype == torch.bfloat16 else KV_FP8_E4M3
+    topk = 0 if topk_indices is None else topk_indices.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().mla_decode_noalloc(
+            _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+            block_table.shape[1], _ptr(cache_seqlens), _ptr(topk_indices), topk, _ptr(kv_scales),
+            float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
     return out, lse
 
 

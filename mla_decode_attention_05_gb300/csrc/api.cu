@@ -92,6 +92,14 @@ WsLayout ws_layout(int n_items, int num_parts) {
 
 }  // namespace
 
+namespace mla {
+// Records the text of an error for mla_last_error_string() (used by the
+// entry points of other translation units).
+void set_last_error(const char *msg) {
+  snprintf(g_err, sizeof g_err, "%s", msg);
+}
+}  // namespace mla
+
 extern "C" {
 
 int mla_default_num_parts(int device) {

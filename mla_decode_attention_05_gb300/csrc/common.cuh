@@ -138,4 +138,5 @@ cudaError_t launch_metadata(const int32_t *seqlens, int B, int H, int T,
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream,
                           cudaEvent_t ev_before, cudaEvent_t ev_after);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream);
+void set_last_error(const char *msg);
 }  // namespace mla
