@@ -120,7 +120,7 @@ int mla_decode_metadata(const int32_t *cache_seqlens, int B, int H, int T,
 /*
  * Bytes of workspace mla_decode needs: fp32 partial outputs and partial LSEs
  * of the split items, (num_items + num_parts) x 128 rows x (512 + 1) floats,
- * plus a ring of 4 x 17.5 KB per worker through which the two SMs of a
+ * plus a ring of 8 x 17.5 KB per worker through which the two SMs of a
  * worker pass the softmax probabilities, each part rounded up to 256 bytes.
  * The workspace needs no initialisation and may be reused by later calls on
  * the same stream (calls that overlap on the GPU need separate workspaces).

@@ -19,7 +19,7 @@ constexpr int MD_STRIDE = 8; // ints per tile_md entry
 constexpr int FP8_ROW = 640; // 512 e4m3 + 64 bf16 RoPE bytes
 // P messages from the S engine to the O engine of a worker pass through a
 // small ring in the workspace (L2-resident): P_RING slots of P_SLOT_BYTES.
-constexpr int P_RING = 4;
+constexpr int P_RING = 8;
 constexpr int P_SLOT_BYTES = 17920;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;

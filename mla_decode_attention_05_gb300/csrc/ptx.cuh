@@ -44,6 +44,19 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Relaxed arrive on another CTA's mbarrier: orders nothing by itself.  After
+// a fence (or with nothing to publish) it is the cheap way to signal; the
+// release form above waits for this thread's prior writes to be performed
+// at cluster scope first.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -124,6 +137,35 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
 // (tensor core / TMA reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named-barrier rendezvous of whole warps that also ORs a flag across the
+// participants (bar.red.or.pred).  Unlike an mbarrier wait it touches no
+// shared memory, so a warp that issues tcgen05.mma can use it without
+// waiting for its MMAs in flight (an mbarrier wait or any shared-memory load
+// by the issuing warp waits for them: measured ~700-950 cycles per wait).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// One lane of the (converged) warp is elected.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
