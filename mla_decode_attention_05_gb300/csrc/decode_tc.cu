@@ -9,12 +9,9 @@
 //
 //   rank 0 ("S engine"): S = Q K^T over all 576 dims (the RoPE block is just
 //          one more block of the reduction, FlashMLA issue #169 "dual gemm"),
-//          on pairs of key tiles so each MMA has N = 128 (full tensor-core
-//          rate; N = 64 runs at about 70 %).  Q dims 0..511 are resident in
-//          TMEM as the A operand, the RoPE block of Q in shared memory, S
-//          double-buffered in TMEM (2 x 128 columns); the online softmax
-//          (conditional rescaling); P in bf16 plus the per-row rescale
-//          factors go to rank 1, one message per tile.
+//          Q resident in TMEM as the A operand, S double-buffered in TMEM;
+//          the online softmax (conditional rescaling); P in bf16 plus the
+//          per-row rescale factors go to rank 1, one message per tile.
 //   rank 1 ("O engine"): O (+)= P V over the 512 latent dims, O resident in
 //          TMEM; applies the rare O rescales; normalises and writes O.
 //
@@ -27,17 +24,16 @@
 // matrices of 8 rows x 16 bytes, 2048 bytes apart along K, 128 along M).  The direct SM-to-SM
 // path (DSMEM) is several times narrower than that per SM.
 //
-// Per CTA, 384 threads:
-//   warp 0      producer: TMA (rank 0: column block kb of both pages of a
-//               group into one 16 KB slot of a 13-slot ring; rank 1: the 8 V blocks of a
-//               page into a 3-stage ring), or with warp 3 the row gather /
-//               FP8 dequantisation into the same layouts
-//   warp 1      TMEM allocation and the MMA-issuing thread
+// Per CTA, 384 threads (416 in the gather kernel):
+//   warp 0      producer: one 4-D TMA per page (rank 0: the 9 column blocks
+//               into a 3-stage ring; rank 1: the 8 V blocks), or with warp 3
+//               the row gather / FP8 dequantisation into the same layout
+//   warp 1      TMEM allocation and the MMA warp (one elected lane issues)
 //   warp 2      rank 0: publishes written P slots to rank 1;
 //               rank 1: P loader (ring slot -> shared memory)
+//   warp 3      the MMA warp's waiter (warp 12 in the gather kernel)
 //   warps 4-11  rank 0: softmax, two threads per query row (TMEM lane):
-//               warps 4-7 take the first tile of each group, warps 8-11 the
-//               second
+//               warps 4-7 take tokens 0-31 of each tile, warps 8-11 32-63
 //               rank 1: O rescale and epilogue, warps 4-7 on O columns
 //               0-255, warps 8-11 on 256-511
 #include <cuda.h>
@@ -59,44 +55,41 @@ __host__ __device__ constexpr int threads_of(bool gather) { return gather ? 416 
 __host__ __device__ constexpr int waiter_warp(bool gather) { return gather ? 12 : 3; }
 constexpr int kSoftmaxWarps = 8;
 constexpr int kBlkBytes = PAGE * 128;             // 64 tokens x 64 dims bf16, 128-byte swizzle
-// rank 0 streams keys in pairs of tiles ("groups"): one slot holds column
-// block kb (64 dims) of both tiles, 128 key rows, so every QK MMA has N = 128
-constexpr int kSlots0 = 13;                       // rank 0: ring of column-block slots
-constexpr int kSlot0Bytes = 2 * kBlkBytes;        // 16384
-constexpr int kStages1 = 3;                       // rank 1: V stages of 8 blocks (one tile)
+constexpr int kStages0 = 3;                       // rank 0: K stages of 9 blocks (one page)
+constexpr int kStage0Bytes = 9 * kBlkBytes;       // 73728
+constexpr int kStages1 = 3;                       // rank 1: V stages of 8 blocks (one page)
 constexpr int kStage1Bytes = 8 * kBlkBytes;       // 65536
 constexpr int kPBytes = M_TILE * 128;             // P tile: 128 rows x 64 tokens bf16
 constexpr int kMetaBytes = 1056;                  // alpha[128], ell[128], flags[8]
 constexpr int kSlotBytes = kPBytes + kMetaBytes;  // one P message (P_SLOT_BYTES apart)
 static_assert(kSlotBytes <= P_SLOT_BYTES, "P ring slot");
-constexpr int kMaskRing = 16;
+constexpr int kMaskRing = 8;
+constexpr int kPublishBatch = 4;                  // P messages published per fence, at most
 constexpr uint64_t kWaitNs = 2000000000ull;       // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // shared memory map (byte offsets from a 1024-aligned base)
 constexpr uint32_t OFF_KV = 0;
-constexpr uint32_t OFF_QROPE = kSlots0 * kSlot0Bytes;               // rank 0: Q RoPE block, 16 KB
-constexpr uint32_t OFF_LPART = OFF_QROPE + M_TILE * 128;            // rank 0: float[2][2][128]
+constexpr uint32_t OFF_LPART = kStages0 * kStage0Bytes;             // rank 0: float[2][2][128]
 constexpr uint32_t OFF_RCV_P = kStages1 * kStage1Bytes;             // rank 1: 196608
 constexpr uint32_t OFF_RCV_META = OFF_RCV_P + 2 * kPBytes;          // rank 1: 229376
 constexpr uint32_t OFF_BARS = OFF_RCV_META + 2 * kMetaBytes;        // 231488
 
 // TMEM columns
-constexpr uint32_t TM_Q = 0;      // rank 0: 256 columns (dims 0..511 as bf16 pairs)
-constexpr uint32_t TM_S = 256;    // rank 0: two S buffers of 128 columns
+constexpr uint32_t TM_Q = 0;      // rank 0: 288 columns (576 bf16 per row)
+constexpr uint32_t TM_S = 320;    // rank 0: two S buffers of 64 columns
 constexpr uint32_t TM_O = 0;      // rank 1: 512 columns
 constexpr uint32_t TM_COLS = 512;
 
-constexpr uint32_t IDESC_QK2 = idesc_bf16_f32(128, 128, false, false);  // group of two tiles
-constexpr uint32_t IDESC_QK1 = idesc_bf16_f32(128, 64, false, false);   // single tile
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
 
 struct Bars {
-  uint64_t kv_full[kSlots0], kv_empty[kSlots0];  // rank 0 slots / rank 1 stages
+  uint64_t kv_full[3], kv_empty[3];
   uint64_t s_full[2], s_free[2];
   uint64_t mfull[kMaskRing];
   uint64_t gfree[P_RING];   // rank 0: ring slot copied out by rank 1
-  uint64_t pwritten[P_RING];// rank 0: the 4 softmax warps of a tile wrote ring slot
+  uint64_t pwritten[P_RING];// rank 0: the 8 softmax warps wrote ring slot
   uint64_t q_ready;
   uint64_t p_full[P_RING];  // rank 1: ring slot published by rank 0
   uint64_t p_land[2];       // rank 1: slot copied into shared buffer b
@@ -112,13 +105,12 @@ struct Bars {
 };
 static_assert(OFF_BARS + sizeof(Bars) <= 232448, "shared memory budget");
 static_assert(OFF_LPART + 4 * M_TILE * 4 <= OFF_BARS, "rank 0 map");
-static_assert(OFF_QROPE % 1024 == 0, "Q RoPE block needs 1024-byte alignment");
 static_assert(OFF_RCV_P % 1024 == 0, "P tiles need 1024-byte alignment");
 
 struct Meta {
   float alpha[M_TILE];
   float ell[M_TILE];
-  uint32_t flags[kSoftmaxWarps];  // [q]: warp q of the writing half rescaled a row (first tile of a group)
+  uint32_t flags[kSoftmaxWarps];  // per softmax warp: any row rescaled in this tile
 };
 static_assert(sizeof(Meta) == kMetaBytes, "meta size");
 
@@ -187,65 +179,34 @@ __device__ __forceinline__ void publish_mask(Bars &br, uint32_t mi, int page, in
 
 // ---- producer: TMA of whole pages ------------------------------------------------
 //
-// rank 0 walks each piece in groups of two tiles (the last group of a piece
-// may hold one): it publishes both tiles' validity masks and loads column
-// block kb of both
-// pages into slot (9 * group + kb) % kSlots0, rows 0-63 from the first page
-// and 64-127 from the second.  rank 1 loads the 512 V dims (8 blocks) of
-// each page into a 3-stage ring.
+// The page pool is viewed as a 4-D tensor [page][9 blocks][64 tokens][64
+// dims] (strides 73728, 128, 1152 bytes), so one TMA box brings a whole page
+// into shared memory as 9 (rank 0) or 8 (rank 1) column blocks of 64 tokens
+// x 128 bytes, 128-byte swizzled: the K-major operand layout.  One
+// instruction per page keeps the producer thread off the critical path.
+// rank 0 also publishes each tile's validity mask.
 
-__device__ void producer_tma0(const Ctx &c, const CUtensorMap *map) {
+__device__ void producer_tma(const Ctx &c, const CUtensorMap *map) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  const uint64_t pol = policy_evict_normal();
+  // rank 1 is the last reader of each page
+  const uint64_t pol = c.rank == 0 ? policy_evict_normal() : policy_evict_first();
+  const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
-  uint32_t g = 0, sl = 0;  // tiles and slots so far
-  for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
-    if (empty) return true;
-    for (int tile = t0; tile < t1; tile += 2) {
-      const int n2 = min(2, t1 - tile);
-      int page[2] = {-1, -1};
-      for (int i = 0; i < n2; i++) {
-        page[i] = page_of(p, it.b, tile + i);
-        publish_mask(br, (g + i) % kMaskRing, page[i], it.kv_len - (tile + i) * PAGE);
-      }
-      for (int kb = 0; kb < 9; kb++, sl++) {
-        const uint32_t s = sl % kSlots0;
-        // An mbarrier wait right after TMA issues stalls the thread for a
-        // few hundred cycles, so wait once per three slots: the commits that
-        // free the slots complete in order, so the third slot being free
-        // means the first two are too.
-        if (kb % 3 == 0) {
-          const uint32_t last = sl + 2;
-          if (!wait_or_abort(c, &br.kv_empty[last % kSlots0], ((last / kSlots0) & 1) ^ 1)) return false;
-        }
-        const uint32_t bar = smem_u32(&br.kv_full[s]);
-        mbar_arrive_expect_tx(bar, (uint32_t)n2 * kBlkBytes);
-        for (int i = 0; i < n2; i++)
-          tma_load_3d(kv0 + s * kSlot0Bytes + i * kBlkBytes, map, bar, kb * 64, 0, page[i] < 0 ? 0 : page[i], pol);
-      }
-      g += n2;
-    }
-    return true;
-  });
-}
-
-__device__ void producer_tma1(const Ctx &c, const CUtensorMap *map) {
-  const DecodeParams &p = *c.p;
-  Bars &br = *c.bars;
-  const uint64_t pol = policy_evict_first();  // rank 1 is the last reader of each page
-  const uint32_t kv0 = smem_u32(c.base + OFF_KV);
-  uint32_t g = 0;
+  uint32_t g = 0, s = 0, ph = 1;  // stage s of tile g; parity of its previous release
   for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t s = g % kStages1;
-      if (!wait_or_abort(c, &br.kv_empty[s], ((g / kStages1) & 1) ^ 1)) return false;
       const int page = page_of(p, it.b, tile);
+      if (c.rank == 0) publish_mask(br, g % kMaskRing, page, it.kv_len - tile * PAGE);
+      if (!wait_or_abort(c, &br.kv_empty[s], ph)) return false;
       const uint32_t bar = smem_u32(&br.kv_full[s]);
-      mbar_arrive_expect_tx(bar, 8u * kBlkBytes);
-      for (int kb = 0; kb < 8; kb++)
-        tma_load_3d(kv0 + s * kStage1Bytes + kb * kBlkBytes, map, bar, kb * 64, 0, page < 0 ? 0 : page, pol);
+      mbar_arrive_expect_tx(bar, stage_bytes);
+      tma_load_4d(kv0 + s * stage_bytes, map, bar, 0, 0, 0, page < 0 ? 0 : page, pol);
+      if (++s == 3) {
+        s = 0;
+        ph ^= 1;
+      }
     }
     return true;
   });
@@ -351,58 +312,43 @@ __device__ __forceinline__ void gather_block(const DecodeParams &p, bool fp8, lo
 }
 
 // Thread pi (0..63) of the gather warps (0 and 3) owns key slot pi of every
-// tile.  rank 0 fills the column-block slots group by group (row pi of both
-// tiles), publishes the masks and writes the gathered-index record; rank 1
-// fills its V stages tile by tile.
+// tile: it resolves the row and writes it, dequantised to bf16, into row pi
+// of each column block of the stage (9 blocks on rank 0, 8 on rank 1).
+// rank 0 also publishes the tile's validity mask and the gathered-index
+// record.
 __device__ void producer_gather(const Ctx &c, int pi) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format == MLA_KV_FP8_E4M3;
+  const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
+  const int nblk = c.rank == 0 ? 9 : 8;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   const int sw = pi & 7;
-  uint32_t g = 0, sl = 0;
+  uint32_t g = 0;
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     const int t_item = (p.topk_len > 0) ? (idx % p.T) : 0;
     const int sk = clamp_seqlen(p.seqlens[it.b], p.status);
-    if (c.rank == 1) {
-      for (int tile = t0; tile < t1; tile++, g++) {
-        const uint32_t s = g % kStages1;
-        if (!wait_or_abort(c, &br.kv_empty[s], ((g / kStages1) & 1) ^ 1)) return false;
-        int n;
-        const long long row = gather_row(p, it, t_item, sk, tile, pi, &n);
-        for (int kb = 0; kb < 8; kb++)
-          gather_block(p, fp8, row, kb, kv0 + s * kStage1Bytes + kb * kBlkBytes + pi * 128, sw);
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&br.kv_full[s]));
-      }
-      return true;
-    }
-    for (int tile = t0; tile < t1; tile += 2) {
-      const int n2 = min(2, t1 - tile);
-      long long row[2] = {-1, -1};
-      for (int i = 0; i < n2; i++) {
-        int n;
-        row[i] = gather_row(p, it, t_item, sk, tile + i, pi, &n);
-        const uint32_t bits = __ballot_sync(0xffffffffu, row[i] >= 0);
-        const uint32_t mi = (g + i) % kMaskRing;
+    for (int tile = t0; tile < t1; tile++, g++) {
+      const uint32_t s = g % 3;
+      int n;
+      const long long row = gather_row(p, it, t_item, sk, tile, pi, &n);
+      if (c.rank == 0) {
+        const uint32_t bits = __ballot_sync(0xffffffffu, row >= 0);
+        const uint32_t mi = g % kMaskRing;
         if ((pi & 31) == 0) br.mask[mi][pi >> 5] = bits;
         if (p.gathered != nullptr && p.topk_len > 0) {
-          const int slot = (tile + i) * PAGE + pi;
+          const int slot = tile * PAGE + pi;
           if (slot < p.topk_len) p.gathered[((size_t)it.b * p.T + t_item) * p.topk_len + slot] = n;
         }
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      for (int kb = 0; kb < 9; kb++, sl++) {
-        const uint32_t s = sl % kSlots0;
-        if (!wait_or_abort(c, &br.kv_empty[s], ((sl / kSlots0) & 1) ^ 1)) return false;
-        for (int i = 0; i < n2; i++)
-          gather_block(p, fp8, row[i], kb, kv0 + s * kSlot0Bytes + i * kBlkBytes + pi * 128, sw);
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&br.kv_full[s]));
-      }
-      g += n2;
+      if (!wait_or_abort(c, &br.kv_empty[s], ((g / 3) & 1) ^ 1)) return false;
+      for (int kb = 0; kb < nblk; kb++)
+        gather_block(p, fp8, row, kb, kv0 + s * stage_bytes + kb * kBlkBytes + pi * 128, sw);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&br.kv_full[s]));
     }
     return true;
   });
@@ -420,18 +366,6 @@ __device__ void producer_gather(const Ctx &c, int pi) {
 constexpr uint32_t kMmaBar = 1;
 constexpr uint32_t kMmaBarThreads = 64;
 
-// ---- rank 0: QK MMA issuer ----------------------------------------------------------
-//
-// Per group j of one or two tiles: S[j&1] = Q . K^T (M = 128, N = 64 per
-// tile, K = 576 in 36 steps of 16).  Steps over dims 0..511 take A = Q from
-// TMEM; the four RoPE steps take A = the Q RoPE block from shared memory.
-// B = column block kb of the slot (K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart, so the second tile's rows continue the first's).  Each
-// slot is released by a commit once its four MMAs are done; S[j&1] is
-// published by a commit after the last.  S is double-buffered, so QK(j+1)
-// overlaps the softmax of j.  Rendezvous with the waiter: once per piece
-// (Q in TMEM) and once per slot (slot full; for kb = 0 also S[j&1] free).
-
 // Lane 0 of a waiter warp has done its waits (ok = all completed); the whole
 // warp meets the MMA warp.  True if either side gives up.
 __device__ __forceinline__ bool waiter_meet(bool ok) {
@@ -439,22 +373,30 @@ __device__ __forceinline__ bool waiter_meet(bool ok) {
   return bar_red_or(kMmaBar, kMmaBarThreads, !ok);
 }
 
+// ---- rank 0: QK MMA issuer ----------------------------------------------------------
+//
+// Per tile g: S[g&1] = Q . K^T (M = 128, N = 64 tokens, K = 576 in 36 steps
+// of 16; A = Q from TMEM, B = the K-major swizzled key blocks of the stage),
+// commit -> kv_empty, s_full.  S is double-buffered, so QK(g+1) overlaps the
+// softmax of g.  The waiter meets the MMA warp once per piece (Q is in
+// TMEM) and once per tile (stage full and S[g&1] free).
+
 __device__ void qk_waiter(const Ctx &c, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  uint32_t j = 0, sl = 0, qn = 0;
+  uint32_t g = 0, qn = 0;
   for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
     if (empty) return true;
     bool ok = true;
     if (lane == 0) ok = wait_or_abort(c, &br.q_ready, qn & 1);
     qn++;
     if (waiter_meet(ok)) return false;
-    for (int tile = t0; tile < t1; tile += 2, j++) {
-      if (lane == 0) ok = wait_or_abort(c, &br.s_free[j & 1], ((j >> 1) & 1) ^ 1);
-      for (int kb = 0; kb < 9; kb++, sl++) {
-        if (lane == 0 && ok) ok = wait_or_abort(c, &br.kv_full[sl % kSlots0], (sl / kSlots0) & 1);
-        if (waiter_meet(ok)) return false;
+    for (int tile = t0; tile < t1; tile++, g++) {
+      if (lane == 0) {
+        ok = wait_or_abort(c, &br.s_free[g & 1], ((g >> 1) & 1) ^ 1);
+        if (ok) ok = wait_or_abort(c, &br.kv_full[g % 3], (g / 3) & 1);
       }
+      if (waiter_meet(ok)) return false;
     }
     return true;
   });
@@ -464,37 +406,30 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
-  const uint64_t qr0 = smem_desc_sw128(smem_u32(c.base + OFF_QROPE), 16, 1024);
   const uint32_t kv_empty0 = smem_u32(&br.kv_empty[0]), s_full0 = smem_u32(&br.s_full[0]);
-  uint32_t j = 0, sl = 0;
+  uint32_t g = 0;
   for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
     if (empty) return true;
     if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // Q is in TMEM
     tc_fence_after();
-    for (int tile = t0; tile < t1; tile += 2, j++) {
-      const uint32_t b = j & 1;
-      const uint32_t idesc = (t1 - tile >= 2) ? IDESC_QK2 : IDESC_QK1;
-      const uint32_t d = tmem + TM_S + b * 128;
-      for (int kb = 0; kb < 9; kb++, sl++) {
-        if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // slot full (and S free)
-        tc_fence_after();
-        const uint32_t s = sl % kSlots0;
-        // step kk only moves the start-address field (16-byte units)
-        const uint64_t kd = smem_desc_sw128(kv0 + s * kSlot0Bytes, 16, 1024);
-        if (elect_one()) {
-          if (kb < 8) {
+    for (int tile = t0; tile < t1; tile++, g++) {
+      const uint32_t s = g % 3, b = g & 1;
+      if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // stage full, S free
+      tc_fence_after();
+      // one base descriptor per tile; block kb / step kk only move its
+      // start-address field (16-byte units: 512 per 8 KB block, 2 per 32 B)
+      const uint64_t kd0 = smem_desc_sw128(kv0 + s * kStage0Bytes, 16, 1024);
+      const uint32_t d = tmem + TM_S + b * 64;
+      if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; kk++)
-              mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd + (uint64_t)(kk * 2), idesc, (kb | kk) ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; kk++) mma_ss(d, qr0 + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc, 1u);
-          }
-          mma_commit(kv_empty0 + s * 8);
-          if (kb == 8) mma_commit(s_full0 + b * 8);
+        for (int i = 0; i < 36; i++) {
+          const int kb = i >> 2, kk = i & 3;
+          mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, i ? 1u : 0u);
         }
-        __syncwarp();
+        mma_commit(kv_empty0 + s * 8);
+        mma_commit(s_full0 + b * 8);
       }
+      __syncwarp();
     }
     return true;
   });
@@ -642,15 +577,13 @@ __device__ __forceinline__ RowInfo row_info(const DecodeParams &p, int idx, cons
   return ri;
 }
 
-// Query row r of the item: thread half 0 puts dims 0..319 (column blocks
-// 0-4) into TMEM columns TM_Q + 32*kb.. as bf16 pairs; half 1 puts blocks
-// 5-7 into TMEM and the RoPE block (dims 512..575) into row r of the
-// shared-memory A operand (K-major, 128-byte swizzle).  Not inlined: once
-// per piece, and inlined its registers would crowd the softmax loop.
-__device__ __noinline__ void load_q(const DecodeParams &p, uint32_t lane_tmem, uint32_t qrope, int r,
-                                       const Item &it, const RowInfo &ri, int hf) {
+// Query row r of the item, column blocks [kb0, kb1) of its 576 dims ->
+// TMEM columns TM_Q + 32*kb.. as bf16 pairs.  Not inlined: it runs once per
+// piece, and inlined its registers would crowd the softmax loop.
+__device__ __noinline__ void load_q(const DecodeParams &p, uint32_t lane_tmem, const Item &it, const RowInfo &ri,
+                                    int kb0, int kb1) {
   const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (((size_t)it.b * p.T + ri.t) * p.H + ri.h) * D_QK);
-  for (int kb = hf ? 5 : 0; kb < (hf ? 8 : 5); kb++) {
+  for (int kb = kb0; kb < kb1; kb++) {
     uint32_t v[32];
 #pragma unroll
     for (int j = 0; j < 8; j++) {
@@ -662,13 +595,6 @@ __device__ __noinline__ void load_q(const DecodeParams &p, uint32_t lane_tmem, u
     }
     tmem_st32(lane_tmem + TM_Q + kb * 32, v);
   }
-  if (hf) {
-    const uint32_t row = qrope + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int j = 0; j < 8; j++)
-      st_shared_v4(row + ((j ^ (r & 7)) << 4), ri.ok ? __ldg(src + 64 + j) : make_uint4(0, 0, 0, 0));
-    fence_proxy_async_smem();
-  }
   tmem_wait_st();
 }
 
@@ -679,6 +605,7 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
   return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
+// Masked-out scores become -inf (skipped when all 32 are valid).
 __device__ __forceinline__ void mask32(float (&v)[32], uint32_t m) {
   if (m != 0xffffffffu) {
 #pragma unroll
@@ -686,23 +613,21 @@ __device__ __forceinline__ void mask32(float (&v)[32], uint32_t m) {
   }
 }
 
-// Thread (q, hf) of warp w = 4 + 4*hf + q owns query row r = 32q + lane and,
-// in each group of two tiles, tile hf (64 keys).  Both threads of a row also
-// read the other tile's scores for its maximum, so they reach the same
-// running max and rescale decisions without talking to each other; each
-// exponentiates its own tile and writes it as one P message (warps 4-7 the
-// first tile's, with the rescale factors; warps 8-11 the second's).  The
-// halves of the row sum meet in shared memory at the last group of a piece.
+// Thread (q, hf) of warp w = 4 + 4*hf + q owns query row r = 32q + lane and
+// tokens [32*hf, 32*hf + 32) of each tile.  Both threads of a row read all 64
+// scores, so they reach the same running max and rescale decisions without
+// talking to each other; each exponentiates and writes its own 32 tokens of
+// the tile's P message and keeps its own part of the row sum.  The halves of
+// the row sum meet in shared memory at the last tile of a piece.
 __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const int q = w & 3, hf = (w - 4) >> 2;
   const int r = q * 32 + lane;
   const uint32_t lt = tmem + ((uint32_t)(q * 32) << 16);
-  const uint32_t qrope = smem_u32(c.base + OFF_QROPE);
   float *lpart = reinterpret_cast<float *>(c.base + OFF_LPART);  // [2 pieces][2 halves][128]
   const float cs = p.scale_log2;
-  uint32_t g = 0, j = 0, pc = 0;
+  uint32_t g = 0, pc = 0;
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int piece, bool empty) {
     const RowInfo ri = row_info(p, idx, it, piece, r);
     float *lse_dst = p.lse + ((size_t)it.b * p.H + ri.h) * p.T + ri.t;
@@ -710,7 +635,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       if (ri.ok && hf == 0) *lse_dst = -INFINITY;
       return true;
     }
-    load_q(p, lt, qrope, r, it, ri, hf);
+    load_q(p, lt, it, ri, hf ? 5 : 0, hf ? 9 : 5);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&br.q_ready));
@@ -719,60 +644,31 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     float m_ref = -INFINITY;  // reference max, raw score units
     float l = 0.f;            // this half's part of the row sum
     float l_all = 0.f;
-    for (int tile = t0; tile < t1; tile += 2, j++) {
-      const int n2 = min(2, t1 - tile);
-      const bool mine = hf < n2;  // warp-uniform
-      const uint32_t b = j & 1;
-      // 1. validity of the group's tiles for this row
-      uint32_t mk[2][2] = {{0u, 0u}, {0u, 0u}};  // [tile of the group][word]
-#pragma unroll
-      for (int i = 0; i < 2; i++) {
-        if (i >= n2) break;
-        const uint32_t mi = (g + i) % kMaskRing;
-        if (!wait_or_abort(c, &br.mfull[mi], ((g + i) / kMaskRing) & 1)) return false;
-        uint32_t lo = br.mask[mi][0], hi = br.mask[mi][1];
-        const int lim = my_len - (tile + i) * PAGE;
-        if (lim < 64) {
-          const uint64_t keep = lim <= 0 ? 0ull : ((1ull << lim) - 1ull);
-          lo &= (uint32_t)keep;
-          hi &= (uint32_t)(keep >> 32);
-        }
-        mk[i][0] = lo;
-        mk[i][1] = hi;
+    for (int tile = t0; tile < t1; tile++, g++) {
+      const uint32_t b = g & 1, u = g >> 1, mi = g % kMaskRing;
+      // 1. tile validity and this row's 64 scores
+      if (!wait_or_abort(c, &br.mfull[mi], (g / kMaskRing) & 1)) return false;
+      uint32_t mlo = br.mask[mi][0], mhi = br.mask[mi][1];
+      const int lim = my_len - tile * PAGE;
+      if (lim < 64) {
+        const uint64_t keep = lim <= 0 ? 0ull : ((1ull << lim) - 1ull);
+        mlo &= (uint32_t)keep;
+        mhi &= (uint32_t)(keep >> 32);
       }
-      if (!wait_or_abort(c, &br.s_full[b], (j >> 1) & 1)) return false;
+      if (!wait_or_abort(c, &br.s_full[b], u & 1)) return false;
       tc_fence_after();
-      // 2. the other tile's maximum, 32 scores at a time, then this tile's
-      //    64 scores (raw units: the scale is positive)
-      // (the masks are selected with the warp-uniform hf, so mk stays in
-      // registers)
-      const uint32_t mown0 = hf ? mk[1][0] : mk[0][0], mown1 = hf ? mk[1][1] : mk[0][1];
-      const uint32_t moth0 = hf ? mk[0][0] : mk[1][0], moth1 = hf ? mk[0][1] : mk[1][1];
-      float mt = -INFINITY;
-      const uint32_t sb = lt + TM_S + b * 128;
-      if ((hf ^ 1) < n2) {  // the other tile exists
-        const uint32_t so = sb + (hf ^ 1) * 64;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; h2++) {
-          float t[32];
-          tmem_ld32(so + h2 * 32, *reinterpret_cast<uint32_t(*)[32]>(&t[0]));
-          tmem_wait_ld();
-          mask32(t, h2 ? moth1 : moth0);
-          mt = fmaxf(mt, max32(t));
-        }
-      }
-      float own0[32], own1[32];
-      if (mine) {
-        tmem_ld32(sb + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&own0[0]));
-        tmem_ld32(sb + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&own1[0]));
-        tmem_wait_ld();
-        mask32(own0, mown0);
-        mask32(own1, mown1);
-        mt = fmaxf(mt, fmaxf(max32(own0), max32(own1)));
-      }
+      float own[32], oth[32];  // this half's 32 scores and the partner half's
+      tmem_ld32(lt + TM_S + b * 64 + hf * 32, *reinterpret_cast<uint32_t(*)[32]>(&own[0]));
+      tmem_ld32(lt + TM_S + b * 64 + (hf ^ 1) * 32, *reinterpret_cast<uint32_t(*)[32]>(&oth[0]));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&br.s_free[b]));
+      // 2. mask (skipped for fully valid tiles) and tile max (raw units; the
+      //    scale is positive)
+      mask32(own, hf ? mhi : mlo);
+      mask32(oth, hf ? mlo : mhi);
+      const float mt = fmaxf(max32(own), max32(oth));
       // 3. conditional rescale: move the reference only when the max grew by
       //    more than 2^8 (FlashAttention-4's conditional rescaling)
       float alpha = 1.f;
@@ -786,47 +682,41 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
         l *= alpha;
       }
       const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref * cs;
-      // 4. P = 2^(s*c - m_ref*c) for this tile -> bf16 into ring slot
-      //    (g + hf) % P_RING, chunk-major (chunk ch of row r at ch*2048 + r*16)
-      const uint32_t gt = g + hf, gs = gt % P_RING;
+      // 4. P = 2^(s*c - m_ref*c) for this half's 32 tokens -> bf16 into ring
+      //    slot g % P_RING, chunk-major (chunk ch of row r at ch*2048 + r*16)
+      const uint32_t gs = g % P_RING;
+      if (!wait_cluster_or_abort(c, &br.gfree[gs], ((g / P_RING) & 1) ^ 1)) return false;
       uint8_t *slot = p.ws_p + ((size_t)c.part * P_RING + gs) * P_SLOT_BYTES;
-      Meta *mo = reinterpret_cast<Meta *>(slot + kPBytes);
-      if (mine) {
-        if (!wait_cluster_or_abort(c, &br.gfree[gs], ((gt / P_RING) & 1) ^ 1)) return false;
-        float psum = 0.f;
+      float psum = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ch++) {
-          const float *src = ch < 4 ? &own0[ch * 8] : &own1[(ch - 4) * 8];
-          uint32_t wv[4];
+      for (int cc = 0; cc < 4; cc++) {
+        const int ch = hf * 4 + cc;
+        uint32_t wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float p0 = ex2(fmaf(src[2 * e], cs, nb));
-            const float p1 = ex2(fmaf(src[2 * e + 1], cs, nb));
-            psum += p0 + p1;
-            wv[e] = pack_bf16(p0, p1);
-          }
-          *reinterpret_cast<uint4 *>(slot + ch * 2048 + r * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        for (int e = 0; e < 4; e++) {
+          const float p0 = ex2(fmaf(own[cc * 8 + 2 * e], cs, nb));
+          const float p1 = ex2(fmaf(own[cc * 8 + 2 * e + 1], cs, nb));
+          psum += p0 + p1;
+          wv[e] = pack_bf16(p0, p1);
         }
-        l += psum;
-        // the group's first message carries the O rescale
-        if (hf == 0) mo->alpha[r] = alpha;
-        const bool any = __any_sync(0xffffffffu, resc);
-        if (lane == 0) mo->flags[q] = (hf == 0 && any) ? 1u : 0u;
+        *reinterpret_cast<uint4 *>(slot + ch * 2048 + r * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
-      if (tile + n2 == t1) {  // last group: both halves of the row sum
+      l += psum;
+      Meta *mo = reinterpret_cast<Meta *>(slot + kPBytes);
+      if (hf == 0) mo->alpha[r] = alpha;
+      const bool any = __any_sync(0xffffffffu, resc);
+      if (lane == 0) mo->flags[w - 4] = any ? 1u : 0u;
+      if (tile == t1 - 1) {  // last tile: both halves of the row sum
         float *lp = lpart + (pc & 1) * 2 * M_TILE;
         lp[hf * M_TILE + r] = l;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&br.lsum[q][pc & 1]));
         if (!wait_or_abort(c, &br.lsum[q][pc & 1], (pc >> 1) & 1)) return false;
         l_all = lp[r] + lp[M_TILE + r];
-        if (mine && tile + hf == t1 - 1) mo->ell[r] = l_all;  // the piece's last message
+        if (hf == 0) mo->ell[r] = l_all;
       }
-      if (mine) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&br.pwritten[gs]));
-      }
-      g += n2;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&br.pwritten[gs]));
     }
     pc++;
     // LSE of this piece (final, natural log; or the split partial, base 2)
@@ -843,29 +733,33 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
 
 // ---- rank 0: P publisher (one thread) ---------------------------------------------------
 //
-// Per group: waits until the softmax warps have written the group's ring
-// slots, makes those writes visible to rank 1 with one fence, and signals
-// each slot with a relaxed remote arrive (fence + relaxed arrive is a
-// release).  One fence per group, off the softmax warps: a fence waits for
-// the stores to reach L2, about 2000 cycles under load.
+// Waits until the eight softmax warps have written ring slot g % P_RING,
+// takes along every following message that is already written (up to
+// kPublishBatch), makes them visible to rank 1 with one fence and signals
+// each with a relaxed remote arrive (fence + relaxed arrive is a release).
+// A fence waits for the stores to reach L2, about 2000 cycles under load;
+// keeping it off the softmax warps and sharing it among messages keeps it
+// off the critical path.
 
 __device__ void p_publisher(const Ctx &c) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const uint32_t pfull1 = mapa(smem_u32(&br.p_full[0]), 1);
-  uint32_t g = 0;
+  uint32_t total = 0;
   for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
-    if (empty) return true;
-    for (int tile = t0; tile < t1; tile += 2) {
-      const int n2 = min(2, t1 - tile);
-      for (int i = 0; i < n2; i++)
-        if (!wait_or_abort(c, &br.pwritten[(g + i) % P_RING], ((g + i) / P_RING) & 1)) return false;
-      fence_acq_rel_cluster();
-      for (int i = 0; i < n2; i++) mbar_arrive_remote_relaxed(pfull1 + ((g + i) % P_RING) * 8);
-      g += n2;
-    }
+    if (!empty) total += (uint32_t)(t1 - t0);
     return true;
   });
+  for (uint32_t g = 0; g < total;) {
+    if (!wait_or_abort(c, &br.pwritten[g % P_RING], (g / P_RING) & 1)) return;
+    uint32_t n = 1;
+    while (n < kPublishBatch && g + n < total &&
+           mbar_test_wait(smem_u32(&br.pwritten[(g + n) % P_RING]), ((g + n) / P_RING) & 1))
+      n++;
+    fence_acq_rel_cluster();
+    for (uint32_t i = 0; i < n; i++) mbar_arrive_remote_relaxed(pfull1 + ((g + i) % P_RING) * 8);
+    g += n;
+  }
 }
 
 // ---- rank 1: O rescale and epilogue (warps 4-11) --------------------------------------------
@@ -895,7 +789,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       const Meta &m = rcv_m[b];
       uint32_t fl = 0;
 #pragma unroll
-      for (int k = 0; k < 4; k++) fl |= m.flags[k];
+      for (int k = 0; k < kSoftmaxWarps; k++) fl |= m.flags[k];
       if (tile == t1 - 1) ell = m.ell[r];
       if (fl != 0u) {  // rare: O *= alpha after PV(g-1), before PV(g)
         const float alpha = m.alpha[r];
@@ -952,7 +846,8 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
 
 template <bool kGather>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather), 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                     const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the shared-memory map needs a 1024-aligned base
     if (threadIdx.x == 0) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
@@ -965,14 +860,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots0; s++) {
+    for (int s = 0; s < 3; s++) {
       mbar_init(smem_u32(&br.kv_full[s]), kGather ? kGatherThreads : 1);
       mbar_init(smem_u32(&br.kv_empty[s]), 1);
     }
     for (int i = 0; i < kMaskRing; i++) mbar_init(smem_u32(&br.mfull[i]), kGather ? 2 : 1);
     for (int i = 0; i < P_RING; i++) {
       mbar_init(smem_u32(&br.gfree[i]), 1);
-      mbar_init(smem_u32(&br.pwritten[i]), kSoftmaxWarps / 2);
+      mbar_init(smem_u32(&br.pwritten[i]), kSoftmaxWarps);
       mbar_init(smem_u32(&br.p_full[i]), 1);
     }
     for (int b = 0; b < 2; b++) {
@@ -993,7 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     tmem_alloc(smem_u32(&br.tmem_base), TM_COLS);
     tmem_relinquish();
   }
-  if (!kGather && threadIdx.x == 0) prefetch_tensormap(&kv_map);
+  if (!kGather && threadIdx.x == 0) prefetch_tensormap(rank == 0 ? (const void *)&k_map : (const void *)&v_map);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1003,8 +898,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   if (kGather) {
     if (warp == 0 || warp == 3) producer_gather(c, warp == 0 ? lane : 32 + lane);
   } else if (warp == 0 && lane == 0) {
-    if (rank == 0) producer_tma0(c, &kv_map);
-    else producer_tma1(c, &kv_map);
+    producer_tma(c, rank == 0 ? &k_map : &v_map);
   }
   if (warp == 1) {
     if (rank == 0) mma_qk(c, tmem);
@@ -1059,21 +953,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_t ev_before,
                           cudaEvent_t ev_after) {
   const bool gather = p.kv_format != MLA_KV_BF16 || p.topk_len > 0;
-  CUtensorMap map;
-  memset(&map, 0, sizeof map);
+  CUtensorMap maps[2];
+  memset(maps, 0, sizeof maps);
   if (!gather) {
-    // The page pool as a 3-D tensor [num_pages][64 tokens][576 dims] of
-    // bf16; one box = 64 dims x 64 tokens of one page, 128-byte swizzle.
+    // The page pool as a 4-D tensor [page][9 blocks][64 tokens][64 dims] of
+    // bf16 (strides 73728, 128 and 1152 bytes); one box = a whole page as 9
+    // (K, rank 0) or 8 (V, rank 1) column blocks, 128-byte swizzle.
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[3] = {(cuuint64_t)D_QK, (cuuint64_t)PAGE, (cuuint64_t)p.num_pages};
-    cuuint64_t strides[2] = {(cuuint64_t)D_QK * 2, (cuuint64_t)D_QK * 2 * PAGE};
-    cuuint32_t box[3] = {64, (cuuint32_t)PAGE, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t *>(p.kv), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    cuuint64_t dims[4] = {64, (cuuint64_t)PAGE, 9, (cuuint64_t)p.num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)D_QK * 2, 128, (cuuint64_t)D_QK * 2 * PAGE};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (int m = 0; m < 2; m++) {
+      cuuint32_t box[4] = {64, (cuuint32_t)PAGE, m == 0 ? 9u : 8u, 1};
+      CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint8_t *>(p.kv), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
   }
   const size_t smem = OFF_BARS + sizeof(Bars);
   auto kern = gather ? decode_tc_kernel<true> : decode_tc_kernel<false>;
@@ -1081,7 +978,7 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.num_parts);
   if (ev_before) cudaEventRecord(ev_before, stream);
-  kern<<<grid, threads_of(gather), smem, stream>>>(map, p);
+  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], p);
   e = cudaGetLastError();
   if (ev_after) cudaEventRecord(ev_after, stream);
   return e;
