@@ -72,8 +72,7 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint32_t OFF_KV = 0;
 constexpr uint32_t OFF_LPART = kStages0 * kStage0Bytes;             // rank 0: float[2][2][128]
 constexpr uint32_t OFF_RCV_P = kStages1 * kStage1Bytes;             // rank 1: 196608
-constexpr uint32_t OFF_RCV_META = OFF_RCV_P + 2 * kPBytes;          // rank 1: 229376
-constexpr uint32_t OFF_BARS = OFF_RCV_META + 2 * kMetaBytes;        // 231488
+constexpr uint32_t OFF_BARS = OFF_RCV_P + 2 * kPBytes;              // 229376
 
 // TMEM columns
 constexpr uint32_t TM_Q = 0;      // rank 0: 288 columns (576 bf16 per row)
@@ -441,13 +440,12 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
 // K=64 tokens in 4 steps; A = P from shared memory, K-major; B = the V
 // blocks of the stage read MN-major).  The first tile of a piece overwrites
 // O.  The waiter meets the MMA warp once per tile, after the V stage is full,
-// P has landed (it then hands the ring slot back to rank 0) and the epilogue
-// warps have applied any rescale (o_ready).
+// P is in shared memory and the epilogue warps have applied any rescale
+// (o_ready).
 
 __device__ void pv_waiter(const Ctx &c, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  const uint32_t gfree0 = mapa(smem_u32(&br.gfree[0]), 0);
   uint32_t g = 0;
   for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
     if (empty) return true;
@@ -457,8 +455,6 @@ __device__ void pv_waiter(const Ctx &c, int lane) {
       if (lane == 0) {
         ok = wait_or_abort(c, &br.kv_full[g % kStages1], (g / kStages1) & 1);
         if (ok) ok = wait_or_abort(c, &br.p_land[b], u & 1);
-        // the slot's bytes are in shared memory: rank 0 may reuse it
-        if (ok) mbar_arrive_remote_relaxed(gfree0 + (g % P_RING) * 8);
         if (ok) ok = wait_or_abort(c, &br.o_ready[b], u & 1);
       }
       if (waiter_meet(ok)) return false;
@@ -502,48 +498,8 @@ __device__ void mma_pv(const Ctx &c, uint32_t tmem) {
   });
 }
 
-// ---- rank 1: P loader ----------------------------------------------------------------
-//
-// Per tile g: wait for rank 0 to publish ring slot g % P_RING and for shared
-// buffer g & 1 to be free (PV(g-2) done); bulk copy the slot (P tile + meta)
-// into the buffer.  The PV issuer hands the slot back to rank 0 once the
-// copy has landed, so copies of consecutive tiles overlap.
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ const uint8_t *ring_slot(const DecodeParams &p, int part, uint32_t g) {
   return p.ws_p + ((size_t)part * P_RING + (g % P_RING)) * P_SLOT_BYTES;
-}
-
-__device__ void p_loader(const Ctx &c) {
-  const DecodeParams &p = *c.p;
-  Bars &br = *c.bars;
-  const uint32_t rcv_p = smem_u32(c.base + OFF_RCV_P), rcv_m = smem_u32(c.base + OFF_RCV_META);
-  uint32_t g = 0;
-  for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
-    if (empty) return true;
-    for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t b = g & 1, u = g >> 1, gs = g % P_RING;
-      if (!wait_cluster_or_abort(c, &br.p_full[gs], (g / P_RING) & 1)) return false;
-      if (!wait_or_abort(c, &br.p_empty[b], (u & 1) ^ 1)) return false;
-      fence_proxy_async_global();
-      const uint8_t *slot = ring_slot(p, c.part, g);
-      const uint32_t land = smem_u32(&br.p_land[b]);
-      mbar_arrive_expect_tx(land, kSlotBytes);
-      bulk_g2s(rcv_p + b * kPBytes, slot, kPBytes, land);
-      bulk_g2s(rcv_m + b * kMetaBytes, slot + kPBytes, kMetaBytes, land);
-    }
-    return true;
-  });
 }
 
 // ---- rank 0: softmax (warps 4-7, thread = query row = TMEM lane) -------------------------
@@ -769,8 +725,10 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
   Bars &br = *c.bars;
   const int q = w & 3, hf = (w - 4) >> 2;
   const int r = q * 32 + lane;
+  const int e = (w - 4) * 32 + lane;  // 0..255: this thread's 16-byte chunks e, e+256, ...
   const uint32_t lt = tmem + ((uint32_t)(q * 32) << 16) + TM_O + hf * 256;
-  const Meta *rcv_m = reinterpret_cast<const Meta *>(c.base + OFF_RCV_META);
+  const uint32_t pbuf = smem_u32(c.base + OFF_RCV_P);
+  const uint32_t gfree0 = mapa(smem_u32(&br.gfree[0]), 0);
   uint32_t g = 0;
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int piece, bool empty) {
     const RowInfo ri = row_info(p, idx, it, piece, r);
@@ -784,15 +742,45 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     }
     float ell = 0.f;
     for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t b = g & 1, u = g >> 1;
-      if (!wait_or_abort(c, &br.p_land[b], u & 1)) return false;
-      const Meta &m = rcv_m[b];
-      uint32_t fl = 0;
+      const uint32_t b = g & 1, u = g >> 1, gs = g % P_RING;
+      // 1. the message is published: load it (P is the 16 KB MMA operand
+      //    image) with plain L2 loads, before waiting for the shared buffer,
+      //    so the L2 latency overlaps PV(g-2).  The bulk-copy engine would
+      //    queue it behind this SM's V loads.  .cg: the slot was rewritten by
+      //    another SM since this SM last read it.
+      if (!wait_cluster_or_abort(c, &br.p_full[gs], (g / P_RING) & 1)) return false;
+      const uint8_t *slot = ring_slot(p, c.part, g);
+      const uint4 *src = reinterpret_cast<const uint4 *>(slot);
+      uint4 v[4];
 #pragma unroll
-      for (int k = 0; k < kSoftmaxWarps; k++) fl |= m.flags[k];
-      if (tile == t1 - 1) ell = m.ell[r];
+      for (int k = 0; k < 4; k++) v[k] = __ldcg(src + e + 256 * k);
+      const Meta *m = reinterpret_cast<const Meta *>(slot + kPBytes);
+      const uint4 f0 = __ldcg(reinterpret_cast<const uint4 *>(m->flags));
+      const uint4 f1 = __ldcg(reinterpret_cast<const uint4 *>(m->flags) + 1);
+      const float alpha = __ldcg(&m->alpha[r]);
+      if (tile == t1 - 1) ell = __ldcg(&m->ell[r]);
+      // 2. shared buffer b is free once PV(g-2) is done
+      if (!wait_or_abort(c, &br.p_empty[b], (u & 1) ^ 1)) return false;
+#pragma unroll
+      for (int k = 0; k < 4; k++) st_shared_v4(pbuf + b * kPBytes + (e + 256 * k) * 16, v[k]);
+      // The slot goes back to rank 0 once this warp's loads are done: the P
+      // chunks are consumed by the stores above, and this instruction
+      // consumes the meta values, so no load is in flight at the arrive.  A
+      // release arrive would also wait for the shared-memory stores and
+      // costs far more.
+      {
+        uint32_t dep;
+        asm volatile("add.u32 %0, %1, %2;" : "=r"(dep) : "r"(__float_as_uint(alpha)), "r"(__float_as_uint(ell)));
+        asm volatile("" ::"r"(dep), "r"(f0.x), "r"(f1.w));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&br.p_land[b]));
+        mbar_arrive_remote_relaxed(gfree0 + gs * 8);
+      }
+      const uint32_t fl = f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w;
       if (fl != 0u) {  // rare: O *= alpha after PV(g-1), before PV(g)
-        const float alpha = m.alpha[r];
         if (!wait_or_abort(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
         tc_fence_after();
         for (int cc = 0; cc < 8; cc++) {
@@ -800,7 +788,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
           tmem_ld32(lt + cc * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int j = 0; j < 32; j++) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
           tmem_st32(lt + cc * 32, o);
         }
         tmem_wait_st();
@@ -866,14 +854,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     }
     for (int i = 0; i < kMaskRing; i++) mbar_init(smem_u32(&br.mfull[i]), kGather ? 2 : 1);
     for (int i = 0; i < P_RING; i++) {
-      mbar_init(smem_u32(&br.gfree[i]), 1);
+      mbar_init(smem_u32(&br.gfree[i]), kSoftmaxWarps);
       mbar_init(smem_u32(&br.pwritten[i]), kSoftmaxWarps);
       mbar_init(smem_u32(&br.p_full[i]), 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(smem_u32(&br.s_full[b]), 1);
       mbar_init(smem_u32(&br.s_free[b]), kSoftmaxWarps);
-      mbar_init(smem_u32(&br.p_land[b]), 1);
+      mbar_init(smem_u32(&br.p_land[b]), kSoftmaxWarps);
       mbar_init(smem_u32(&br.p_empty[b]), 1);
       mbar_init(smem_u32(&br.o_ready[b]), kSoftmaxWarps);
       mbar_init(smem_u32(&br.o_done[b]), 1);
@@ -908,10 +896,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     if (rank == 0) qk_waiter(c, lane);
     else pv_waiter(c, lane);
   }
-  if (warp == 2 && lane == 0) {
-    if (rank == 0) p_publisher(c);
-    else p_loader(c);
-  }
+  if (warp == 2 && lane == 0 && rank == 0) p_publisher(c);
   if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
     if (rank == 0) softmax_role(c, tmem, warp, lane);
     else epilogue_role(c, tmem, warp, lane);
