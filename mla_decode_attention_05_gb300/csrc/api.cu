@@ -222,6 +222,7 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   p.n_mt = n_mt_of(H, T);
   p.n_items = n_items;
   p.num_parts = num_parts;
+  p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.scale_log2 = softmax_scale * mla::LOG2E;
 
   cudaStream_t s = (cudaStream_t)stream;

@@ -50,6 +50,7 @@ struct DecodeParams {
   int n_mt;     // M tiles per sequence (dense / causal)
   int n_items;
   int num_parts;
+  int out_v8;        // out is 32-byte aligned: 32-byte stores
   float scale_log2;  // softmax_scale * log2(e)
 };
 

@@ -153,6 +153,10 @@ __device__ __forceinline__ bool for_each_piece(const DecodeParams &p, int part, 
 
 // Page of key tile `tile` of sequence b, or -1 (status bit set) if the
 // block table entry is outside the pool.
+// rank 0's stage ring carries, per piece, the item's query rows (one stage
+// per 64 rows, loaded by TMA in the K layout) before its key tiles.
+__device__ __forceinline__ int q_stages(const Item &it) { return it.rows > 64 ? 2 : 1; }
+
 __device__ __forceinline__ int page_of(const DecodeParams &p, int b, int tile) {
   if (tile >= p.max_pages) {
     atomicOr(p.status, MLA_STATUS_BAD_SEQLEN);
@@ -185,7 +189,7 @@ __device__ __forceinline__ void publish_mask(Bars &br, uint32_t mi, int page, in
 // instruction per page keeps the producer thread off the critical path.
 // rank 0 also publishes each tile's validity mask.
 
-__device__ void producer_tma(const Ctx &c, const CUtensorMap *map) {
+__device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtensorMap *q_map, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   // rank 1 is the last reader of each page
@@ -195,16 +199,50 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map) {
   uint32_t g = 0, s = 0, ph = 1;  // stage s of tile g; parity of its previous release
   for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
-    for (int tile = t0; tile < t1; tile++, g++) {
-      const int page = page_of(p, it.b, tile);
-      if (c.rank == 0) publish_mask(br, g % kMaskRing, page, it.kv_len - tile * PAGE);
-      if (!wait_or_abort(c, &br.kv_empty[s], ph)) return false;
-      const uint32_t bar = smem_u32(&br.kv_full[s]);
-      mbar_arrive_expect_tx(bar, stage_bytes);
-      tma_load_4d(kv0 + s * stage_bytes, map, bar, 0, 0, 0, page < 0 ? 0 : page, pol);
-      if (++s == 3) {
-        s = 0;
-        ph ^= 1;
+    if (c.rank == 0) {
+      // the item's query rows are contiguous (row0 .. row0+rows-1 of
+      // sequence b): one or two boxes of 64 rows x 9 blocks
+      const int qrow = it.b * p.T * p.H + it.row0;
+      for (int qh = 0; qh < q_stages(it); qh++) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_or_abort(c, &br.kv_empty[s], ph);
+          if (ok) {
+            const uint32_t bar = smem_u32(&br.kv_full[s]);
+            mbar_arrive_expect_tx(bar, kStage0Bytes);
+            tma_load_3d(kv0 + s * kStage0Bytes, q_map, bar, 0, qrow + 64 * qh, 0, policy_evict_first());
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        if (++s == 3) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+    // The whole warp reads the block-table entries of up to 32 tiles at once
+    // (a lone lane would pay a global-memory round trip per tile); lane 0
+    // issues the copies.
+    for (int base = t0; base < t1; base += 32) {
+      const int pg = (base + lane < t1) ? page_of(p, it.b, base + lane) : -1;
+      const int cnt = min(32, t1 - base);
+      for (int i = 0; i < cnt; i++, g++) {
+        const int page = __shfl_sync(0xffffffffu, pg, i);
+        bool ok = true;
+        if (lane == 0) {
+          if (c.rank == 0) publish_mask(br, g % kMaskRing, page, it.kv_len - (base + i) * PAGE);
+          ok = wait_or_abort(c, &br.kv_empty[s], ph);
+          if (ok) {
+            const uint32_t bar = smem_u32(&br.kv_full[s]);
+            mbar_arrive_expect_tx(bar, stage_bytes);
+            tma_load_4d(kv0 + s * stage_bytes, map, bar, 0, 0, 0, page < 0 ? 0 : page, pol);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        if (++s == 3) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
     return true;
@@ -315,7 +353,7 @@ __device__ __forceinline__ void gather_block(const DecodeParams &p, bool fp8, lo
 // of each column block of the stage (9 blocks on rank 0, 8 on rank 1).
 // rank 0 also publishes the tile's validity mask and the gathered-index
 // record.
-__device__ void producer_gather(const Ctx &c, int pi) {
+__device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format == MLA_KV_FP8_E4M3;
@@ -323,13 +361,27 @@ __device__ void producer_gather(const Ctx &c, int pi) {
   const int nblk = c.rank == 0 ? 9 : 8;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   const int sw = pi & 7;
-  uint32_t g = 0;
+  uint32_t g = 0, sq = 0;  // tiles; stages of the ring (rank 0: query stages too)
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     const int t_item = (p.topk_len > 0) ? (idx % p.T) : 0;
     const int sk = clamp_seqlen(p.seqlens[it.b], p.status);
-    for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t s = g % 3;
+    if (c.rank == 0) {  // the query rows, by TMA (thread 0 issues, all 64 arrive)
+      const int qrow = it.b * p.T * p.H + it.row0;
+      for (int qh = 0; qh < q_stages(it); qh++, sq++) {
+        const uint32_t s = sq % 3;
+        if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
+        const uint32_t bar = smem_u32(&br.kv_full[s]);
+        if (pi == 0) {
+          mbar_arrive_expect_tx(bar, kStage0Bytes);
+          tma_load_3d(kv0 + s * kStage0Bytes, q_map, bar, 0, qrow + 64 * qh, 0, policy_evict_first());
+        } else {
+          mbar_arrive(bar);
+        }
+      }
+    }
+    for (int tile = t0; tile < t1; tile++, g++, sq++) {
+      const uint32_t s = sq % 3;
       int n;
       const long long row = gather_row(p, it, t_item, sk, tile, pi, &n);
       if (c.rank == 0) {
@@ -343,7 +395,7 @@ __device__ void producer_gather(const Ctx &c, int pi) {
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      if (!wait_or_abort(c, &br.kv_empty[s], ((g / 3) & 1) ^ 1)) return false;
+      if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
       for (int kb = 0; kb < nblk; kb++)
         gather_block(p, fp8, row, kb, kv0 + s * stage_bytes + kb * kBlkBytes + pi * 128, sw);
       fence_proxy_async_smem();
@@ -383,17 +435,18 @@ __device__ __forceinline__ bool waiter_meet(bool ok) {
 __device__ void qk_waiter(const Ctx &c, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  uint32_t g = 0, qn = 0;
-  for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
+  uint32_t g = 0, qn = 0, sq = 0;  // tiles, pieces, ring stages
+  for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     bool ok = true;
     if (lane == 0) ok = wait_or_abort(c, &br.q_ready, qn & 1);
     qn++;
+    sq += q_stages(it);  // the query stages, read by the softmax warps
     if (waiter_meet(ok)) return false;
-    for (int tile = t0; tile < t1; tile++, g++) {
+    for (int tile = t0; tile < t1; tile++, g++, sq++) {
       if (lane == 0) {
         ok = wait_or_abort(c, &br.s_free[g & 1], ((g >> 1) & 1) ^ 1);
-        if (ok) ok = wait_or_abort(c, &br.kv_full[g % 3], (g / 3) & 1);
+        if (ok) ok = wait_or_abort(c, &br.kv_full[sq % 3], (sq / 3) & 1);
       }
       if (waiter_meet(ok)) return false;
     }
@@ -406,13 +459,19 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
   Bars &br = *c.bars;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   const uint32_t kv_empty0 = smem_u32(&br.kv_empty[0]), s_full0 = smem_u32(&br.s_full[0]);
-  uint32_t g = 0;
-  for_each_piece(p, c.part, [&](int, const Item &, int t0, int t1, int, bool empty) {
+  uint32_t g = 0, sq = 0;  // tiles, ring stages
+  for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // Q is in TMEM
     tc_fence_after();
-    for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t s = g % 3, b = g & 1;
+    // the softmax warps have copied the query stages into TMEM: release them
+    // (the commit arrives once the MMAs issued so far are done)
+    if (elect_one())
+      for (int qh = 0; qh < q_stages(it); qh++) mma_commit(kv_empty0 + ((sq + qh) % 3) * 8);
+    __syncwarp();
+    sq += q_stages(it);
+    for (int tile = t0; tile < t1; tile++, g++, sq++) {
+      const uint32_t s = sq % 3, b = g & 1;
       if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // stage full, S free
       tc_fence_after();
       // one base descriptor per tile; block kb / step kk only move its
@@ -534,16 +593,21 @@ __device__ __forceinline__ RowInfo row_info(const DecodeParams &p, int idx, cons
 }
 
 // Query row r of the item, column blocks [kb0, kb1) of its 576 dims ->
-// TMEM columns TM_Q + 32*kb.. as bf16 pairs.  Not inlined: it runs once per
-// piece, and inlined its registers would crowd the softmax loop.
-__device__ __noinline__ void load_q(const DecodeParams &p, uint32_t lane_tmem, const Item &it, const RowInfo &ri,
-                                    int kb0, int kb1) {
-  const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (((size_t)it.b * p.T + ri.t) * p.H + ri.h) * D_QK);
+// TMEM columns TM_Q + 32*kb.. as bf16 pairs, from the ring stage that holds
+// the item's rows 64*(r/64) .. (K-major 128-byte swizzled layout: row rr of
+// block kb at kb*8192 + rr*128, 16-byte chunk j at (j ^ (rr & 7)) * 16).
+// Rows past the item get zeros.  Not inlined: it runs once per piece, and
+// inlined its registers would crowd the softmax loop.
+__device__ __noinline__ void load_q(uint32_t lane_tmem, uint32_t stage, int rr, bool ok, int kb0, int kb1) {
   for (int kb = kb0; kb < kb1; kb++) {
     uint32_t v[32];
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-      const uint4 x = ri.ok ? __ldg(src + kb * 8 + j) : make_uint4(0, 0, 0, 0);
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (ok)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                     : "r"(stage + kb * kBlkBytes + rr * 128 + ((j ^ (rr & 7)) << 4)));
       v[4 * j] = x.x;
       v[4 * j + 1] = x.y;
       v[4 * j + 2] = x.z;
@@ -583,7 +647,8 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
   const uint32_t lt = tmem + ((uint32_t)(q * 32) << 16);
   float *lpart = reinterpret_cast<float *>(c.base + OFF_LPART);  // [2 pieces][2 halves][128]
   const float cs = p.scale_log2;
-  uint32_t g = 0, pc = 0;
+  const uint32_t kv0 = smem_u32(c.base + OFF_KV);
+  uint32_t g = 0, pc = 0, sq = 0;  // tiles, pieces, ring stages
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int piece, bool empty) {
     const RowInfo ri = row_info(p, idx, it, piece, r);
     float *lse_dst = p.lse + ((size_t)it.b * p.H + ri.h) * p.T + ri.t;
@@ -591,7 +656,12 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       if (ri.ok && hf == 0) *lse_dst = -INFINITY;
       return true;
     }
-    load_q(p, lt, it, ri, hf ? 5 : 0, hf ? 9 : 5);
+    {  // the query rows, from the stage ring into TMEM
+      const uint32_t qs = sq + (r >> 6);  // rows past the item (ri.ok false) read nothing
+      if (ri.ok && !wait_or_abort(c, &br.kv_full[qs % 3], (qs / 3) & 1)) return false;
+      load_q(lt, kv0 + (qs % 3) * kStage0Bytes, r & 63, ri.ok, hf ? 5 : 0, hf ? 9 : 5);
+      sq += q_stages(it) + (t1 - t0);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&br.q_ready));
@@ -803,27 +873,30 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     tc_fence_after();
     const float inv = ell > 0.f ? 1.f / ell : 0.f;
     float *wrow = p.ws_o + (ri.slot * M_TILE + r) * D_V + hf * 256;
+    // 32-byte stores: each lane writes whole L2 sectors of its row
     for (int cc = 0; cc < 8; cc++) {
       uint32_t o[32];
       tmem_ld32(lt + cc * 32, o);
       tmem_wait_ld();
       if (!ri.ok) continue;
       if (ri.nsplit <= 1) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const int e = 8 * j;
-          dst[j] = make_uint4(pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
-                              pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
-                              pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
-                              pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+        for (int j = 0; j < 16; j++) w[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+        __nv_bfloat16 *dst = orow + cc * 32;
+        if (p.out_v8) {
+          st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+          st_global_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+        } else {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+          for (int j = 0; j < 4; j++) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       } else {
-        float4 *dst = reinterpret_cast<float4 *>(wrow + cc * 32);
 #pragma unroll
-        for (int j = 0; j < 8; j++)
-          dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                               __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        for (int j = 0; j < 32; j++) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
+#pragma unroll
+        for (int j = 0; j < 4; j++) st_global_v8(wrow + cc * 32 + 8 * j, *reinterpret_cast<const uint32_t(*)[8]>(&o[8 * j]));
       }
     }
     return true;
@@ -835,7 +908,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
 template <bool kGather>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
-                     const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the shared-memory map needs a 1024-aligned base
     if (threadIdx.x == 0) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
@@ -884,9 +957,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   const uint32_t tmem = br.tmem_base;
 
   if (kGather) {
-    if (warp == 0 || warp == 3) producer_gather(c, warp == 0 ? lane : 32 + lane);
-  } else if (warp == 0 && lane == 0) {
-    producer_tma(c, rank == 0 ? &k_map : &v_map);
+    if (warp == 0 || warp == 3) producer_gather(c, &q_map, warp == 0 ? lane : 32 + lane);
+  } else if (warp == 0) {
+    producer_tma(c, rank == 0 ? &k_map : &v_map, &q_map, lane);
   }
   if (warp == 1) {
     if (rank == 0) mma_qk(c, tmem);
@@ -938,17 +1011,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_t ev_before,
                           cudaEvent_t ev_after) {
   const bool gather = p.kv_format != MLA_KV_BF16 || p.topk_len > 0;
-  CUtensorMap maps[2];
+  CUtensorMap maps[3];
   memset(maps, 0, sizeof maps);
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   if (!gather) {
     // The page pool as a 4-D tensor [page][9 blocks][64 tokens][64 dims] of
     // bf16 (strides 73728, 128 and 1152 bytes); one box = a whole page as 9
     // (K, rank 0) or 8 (V, rank 1) column blocks, 128-byte swizzle.
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[4] = {64, (cuuint64_t)PAGE, 9, (cuuint64_t)p.num_pages};
     cuuint64_t strides[3] = {(cuuint64_t)D_QK * 2, 128, (cuuint64_t)D_QK * 2 * PAGE};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
     for (int m = 0; m < 2; m++) {
       cuuint32_t box[4] = {64, (cuuint32_t)PAGE, m == 0 ? 9u : 8u, 1};
       CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint8_t *>(p.kv), dims, strides,
@@ -957,13 +1030,25 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
   }
+  {
+    // The queries as a 3-D tensor [9 blocks][B*T*H rows][64 dims] (strides
+    // 128 and 1152 bytes); one box = 64 query rows in the K layout.  Rows
+    // past the end read as zeros.
+    cuuint64_t dims[3] = {64, (cuuint64_t)p.B * p.T * p.H, 9};
+    cuuint64_t strides[2] = {(cuuint64_t)D_QK * 2, 128};
+    cuuint32_t box[3] = {64, 64, 9};
+    CUresult r = fn(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(p.q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   const size_t smem = OFF_BARS + sizeof(Bars);
   auto kern = gather ? decode_tc_kernel<true> : decode_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.num_parts);
   if (ev_before) cudaEventRecord(ev_before, stream);
-  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], p);
+  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], maps[2], p);
   e = cudaGetLastError();
   if (ev_after) cudaEventRecord(ev_after, stream);
   return e;

@@ -311,6 +311,14 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 32-byte global stores (sm_100 family): one full L2 sector per lane.  The
+// address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ---- descriptors ----------------------------------------------------------------
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
