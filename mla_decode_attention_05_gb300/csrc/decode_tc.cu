@@ -84,7 +84,8 @@ constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
 
 struct Bars {
-  uint64_t kv_full[3], kv_empty[3];
+  uint64_t kv_full[3], kv_empty[3];      // rank 0: blocks 0-4 of a K stage; rank 1: V stages
+  uint64_t kv_full_b[3], kv_empty_b[3];  // rank 0: blocks 5-8 of a K stage
   uint64_t s_full[2], s_free[2];
   uint64_t mfull[kMaskRing];
   uint64_t gfree[P_RING];   // rank 0: ring slot copied out by rank 1
@@ -189,7 +190,11 @@ __device__ __forceinline__ void publish_mask(Bars &br, uint32_t mi, int page, in
 // instruction per page keeps the producer thread off the critical path.
 // rank 0 also publishes each tile's validity mask.
 
-__device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtensorMap *q_map, int lane) {
+// rank 0 loads each K page as two boxes, blocks 0-4 and 5-8, with their own
+// barriers, so the first half of a stage can be refilled as soon as the QK
+// MMAs that read it are done (about half a tile earlier than the whole).
+__device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtensorMap *map_b,
+                             const CUtensorMap *q_map, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   // rank 1 is the last reader of each page
@@ -206,11 +211,12 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
       for (int qh = 0; qh < q_stages(it); qh++) {
         bool ok = true;
         if (lane == 0) {
-          ok = wait_or_abort(c, &br.kv_empty[s], ph);
+          ok = wait_or_abort(c, &br.kv_empty[s], ph) && wait_or_abort(c, &br.kv_empty_b[s], ph);
           if (ok) {
             const uint32_t bar = smem_u32(&br.kv_full[s]);
             mbar_arrive_expect_tx(bar, kStage0Bytes);
             tma_load_3d(kv0 + s * kStage0Bytes, q_map, bar, 0, qrow + 64 * qh, 0, policy_evict_first());
+            mbar_arrive(smem_u32(&br.kv_full_b[s]));  // the whole stage is in the first box
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
@@ -234,8 +240,17 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
           ok = wait_or_abort(c, &br.kv_empty[s], ph);
           if (ok) {
             const uint32_t bar = smem_u32(&br.kv_full[s]);
-            mbar_arrive_expect_tx(bar, stage_bytes);
+            const uint32_t bytes = c.rank == 0 ? 5 * kBlkBytes : stage_bytes;
+            mbar_arrive_expect_tx(bar, bytes);
             tma_load_4d(kv0 + s * stage_bytes, map, bar, 0, 0, 0, page < 0 ? 0 : page, pol);
+          }
+          if (ok && c.rank == 0) {
+            ok = wait_or_abort(c, &br.kv_empty_b[s], ph);
+            if (ok) {
+              const uint32_t bar = smem_u32(&br.kv_full_b[s]);
+              mbar_arrive_expect_tx(bar, 4 * kBlkBytes);
+              tma_load_4d(kv0 + s * stage_bytes + 5 * kBlkBytes, map_b, bar, 0, 0, 5, page < 0 ? 0 : page, pol);
+            }
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
@@ -371,6 +386,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
       for (int qh = 0; qh < q_stages(it); qh++, sq++) {
         const uint32_t s = sq % 3;
         if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
+        if (!wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1)) return false;
         const uint32_t bar = smem_u32(&br.kv_full[s]);
         if (pi == 0) {
           mbar_arrive_expect_tx(bar, kStage0Bytes);
@@ -378,6 +394,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         } else {
           mbar_arrive(bar);
         }
+        mbar_arrive(smem_u32(&br.kv_full_b[s]));
       }
     }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
@@ -396,10 +413,12 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
       if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
+      if (c.rank == 0 && !wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1)) return false;
       for (int kb = 0; kb < nblk; kb++)
         gather_block(p, fp8, row, kb, kv0 + s * stage_bytes + kb * kBlkBytes + pi * 128, sw);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
+      if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
     }
     return true;
   });
@@ -448,7 +467,9 @@ __device__ void qk_waiter(const Ctx &c, int lane) {
         ok = wait_or_abort(c, &br.s_free[g & 1], ((g >> 1) & 1) ^ 1);
         if (ok) ok = wait_or_abort(c, &br.kv_full[sq % 3], (sq / 3) & 1);
       }
-      if (waiter_meet(ok)) return false;
+      if (waiter_meet(ok)) return false;  // blocks 0-4 of the stage, S free
+      if (lane == 0) ok = wait_or_abort(c, &br.kv_full_b[sq % 3], (sq / 3) & 1);
+      if (waiter_meet(ok)) return false;  // blocks 5-8
     }
     return true;
   });
@@ -459,6 +480,7 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
   Bars &br = *c.bars;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   const uint32_t kv_empty0 = smem_u32(&br.kv_empty[0]), s_full0 = smem_u32(&br.s_full[0]);
+  const uint32_t kv_empty_b0 = smem_u32(&br.kv_empty_b[0]);
   uint32_t g = 0, sq = 0;  // tiles, ring stages
   for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
@@ -467,12 +489,15 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
     // the softmax warps have copied the query stages into TMEM: release them
     // (the commit arrives once the MMAs issued so far are done)
     if (elect_one())
-      for (int qh = 0; qh < q_stages(it); qh++) mma_commit(kv_empty0 + ((sq + qh) % 3) * 8);
+      for (int qh = 0; qh < q_stages(it); qh++) {
+        mma_commit(kv_empty0 + ((sq + qh) % 3) * 8);
+        mma_commit(kv_empty_b0 + ((sq + qh) % 3) * 8);
+      }
     __syncwarp();
     sq += q_stages(it);
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
       const uint32_t s = sq % 3, b = g & 1;
-      if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // stage full, S free
+      if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // blocks 0-4 in, S free
       tc_fence_after();
       // one base descriptor per tile; block kb / step kk only move its
       // start-address field (16-byte units: 512 per 8 KB block, 2 per 32 B)
@@ -480,11 +505,22 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
       const uint32_t d = tmem + TM_S + b * 64;
       if (elect_one()) {
 #pragma unroll
-        for (int i = 0; i < 36; i++) {
+        for (int i = 0; i < 20; i++) {
           const int kb = i >> 2, kk = i & 3;
           mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, i ? 1u : 0u);
         }
         mma_commit(kv_empty0 + s * 8);
+      }
+      __syncwarp();
+      if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // blocks 5-8 in
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int i = 20; i < 36; i++) {
+          const int kb = i >> 2, kk = i & 3;
+          mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, 1u);
+        }
+        mma_commit(kv_empty_b0 + s * 8);
         mma_commit(s_full0 + b * 8);
       }
       __syncwarp();
@@ -907,8 +943,9 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
 
 template <bool kGather>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather), 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
-                     const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap kb_map,
+                     const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap q_map,
+                     const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the shared-memory map needs a 1024-aligned base
     if (threadIdx.x == 0) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
@@ -924,6 +961,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     for (int s = 0; s < 3; s++) {
       mbar_init(smem_u32(&br.kv_full[s]), kGather ? kGatherThreads : 1);
       mbar_init(smem_u32(&br.kv_empty[s]), 1);
+      mbar_init(smem_u32(&br.kv_full_b[s]), kGather ? kGatherThreads : 1);
+      mbar_init(smem_u32(&br.kv_empty_b[s]), 1);
     }
     for (int i = 0; i < kMaskRing; i++) mbar_init(smem_u32(&br.mfull[i]), kGather ? 2 : 1);
     for (int i = 0; i < P_RING; i++) {
@@ -959,7 +998,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   if (kGather) {
     if (warp == 0 || warp == 3) producer_gather(c, &q_map, warp == 0 ? lane : 32 + lane);
   } else if (warp == 0) {
-    producer_tma(c, rank == 0 ? &k_map : &v_map, &q_map, lane);
+    producer_tma(c, rank == 0 ? &k_map : &v_map, &kb_map, &q_map, lane);
   }
   if (warp == 1) {
     if (rank == 0) mma_qk(c, tmem);
@@ -1011,19 +1050,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_t ev_before,
                           cudaEvent_t ev_after) {
   const bool gather = p.kv_format != MLA_KV_BF16 || p.topk_len > 0;
-  CUtensorMap maps[3];
+  CUtensorMap maps[4];
   memset(maps, 0, sizeof maps);
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   if (!gather) {
     // The page pool as a 4-D tensor [page][9 blocks][64 tokens][64 dims] of
-    // bf16 (strides 73728, 128 and 1152 bytes); one box = a whole page as 9
-    // (K, rank 0) or 8 (V, rank 1) column blocks, 128-byte swizzle.
+    // bf16 (strides 73728, 128 and 1152 bytes); a box = column blocks 0-4 or
+    // 5-8 of a page (K, rank 0) or blocks 0-7 (V, rank 1), 128-byte swizzle.
     cuuint64_t dims[4] = {64, (cuuint64_t)PAGE, 9, (cuuint64_t)p.num_pages};
     cuuint64_t strides[3] = {(cuuint64_t)D_QK * 2, 128, (cuuint64_t)D_QK * 2 * PAGE};
-    for (int m = 0; m < 2; m++) {
-      cuuint32_t box[4] = {64, (cuuint32_t)PAGE, m == 0 ? 9u : 8u, 1};
+    const cuuint32_t nblk[3] = {5, 4, 8};  // K blocks 0-4, K blocks 5-8, V
+    for (int m = 0; m < 3; m++) {
+      cuuint32_t box[4] = {64, (cuuint32_t)PAGE, nblk[m], 1};
       CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint8_t *>(p.kv), dims, strides,
                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1037,7 +1077,7 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
     cuuint64_t dims[3] = {64, (cuuint64_t)p.B * p.T * p.H, 9};
     cuuint64_t strides[2] = {(cuuint64_t)D_QK * 2, 128};
     cuuint32_t box[3] = {64, 64, 9};
-    CUresult r = fn(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(p.q), dims, strides,
+    CUresult r = fn(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(p.q), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -1048,7 +1088,7 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.num_parts);
   if (ev_before) cudaEventRecord(ev_before, stream);
-  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], maps[2], p);
+  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
   e = cudaGetLastError();
   if (ev_after) cudaEventRecord(ev_after, stream);
   return e;
