@@ -86,6 +86,7 @@ constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
 struct Bars {
   uint64_t kv_full[3], kv_empty[3];      // rank 0: blocks 0-4 of a K stage; rank 1: V stages
   uint64_t kv_full_b[3], kv_empty_b[3];  // rank 0: blocks 5-8 of a K stage
+  uint64_t raw_full[3];                  // gather kernel: the stage's raw FP8 rows landed
   uint64_t s_full[2], s_free[2];
   uint64_t mfull[kMaskRing];
   uint64_t gfree[P_RING];   // rank 0: ring slot copied out by rank 1
@@ -326,41 +327,101 @@ __device__ __forceinline__ long long gather_row(const DecodeParams &p, const Ite
   return row;
 }
 
-// Column block kb (dims 64kb .. 64kb+63) of pool row `row` (zeros for -1),
-// as bf16 into the 128-byte swizzled row at shared address dst (row pi of a
-// block: chunk j at ((j ^ (pi & 7)) << 4)).
-__device__ __forceinline__ void gather_block(const DecodeParams &p, bool fp8, long long row, int kb, uint32_t dst,
-                                             int sw) {
+// 16-byte asynchronous copy global -> shared (cp.async); with ok false it
+// writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+constexpr uint32_t kGatherBar = 2;  // named barrier of the 64 gather threads
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Row pi of one tile: pool row `row` (zeros for -1) into the stage at
+// shared address st, as bf16 column blocks 0-7 (+ the RoPE block 8 when
+// rope), 128-byte swizzled (row pi of block kb at kb*8192 + pi*128, chunk j
+// at ((j ^ (pi & 7)) << 4)).
+//
+// FP8 rows: each thread brings its whole row (640 bytes on rank 0, the 512
+// e4m3 bytes on rank 1) with one bulk copy into a raw staging area at the
+// start of the stage (row pi at pi * rowbytes), completing on raw_bar;
+// thousands of 16-byte requests for random rows would leave the SM only a
+// few KB in flight.  Then each thread dequantises its row: the blocks that
+// lie past the staging area first, then, after all 64 threads have read
+// their staged bytes into registers, the blocks that overwrite it.
+// bf16 rows are copied 16 bytes at a time straight into place.
+__device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long long row, uint32_t st, int pi,
+                                                    bool rope, uint64_t *raw_bar, uint32_t raw_par) {
+  const DecodeParams &p = *c.p;
   const bool ok = row >= 0;
-  if (fp8) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.kv + (ok ? row : 0) * FP8_ROW);
-    if (kb < 8) {  // 64 e4m3 values, one per-128 scale
-      uint4 v[4];
+  const int sw = pi & 7;
+  if (!fp8) {
+    const uint8_t *src = p.kv + (ok ? row : 0) * (D_QK * 2);
+    const int nb = rope ? 9 : 8;
+    for (int kb = 0; kb < nb; kb++)
 #pragma unroll
-      for (int j = 0; j < 4; j++) v[j] = ok ? __ldg(src + kb * 4 + j) : make_uint4(0, 0, 0, 0);
-      const float scale = ok ? __ldg(p.kv_scales + row * 4 + (kb >> 1)) : 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        uint4 lo, hi;
-        dequant16(v[j], scale, lo, hi);
-        st_shared_v4(dst + (((2 * j) ^ sw) << 4), lo);
-        st_shared_v4(dst + (((2 * j + 1) ^ sw) << 4), hi);
-      }
-    } else {  // RoPE: 64 bf16 after the 512 e4m3 bytes
-      uint4 v[8];
-#pragma unroll
-      for (int j = 0; j < 8; j++) v[j] = ok ? __ldg(src + 32 + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 8; j++) st_shared_v4(dst + ((j ^ sw) << 4), v[j]);
-    }
-  } else {
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.kv + (ok ? row : 0) * (D_QK * 2));
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) v[j] = ok ? __ldg(src + kb * 8 + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < 8; j++) st_shared_v4(dst + ((j ^ sw) << 4), v[j]);
+      for (int j = 0; j < 8; j++) cp_async16(st + kb * kBlkBytes + pi * 128 + ((j ^ sw) << 4), src + kb * 128 + j * 16, ok);
+    cp_async_wait_all();
+    return true;
   }
+  const uint32_t rowbytes = rope ? FP8_ROW : 512;
+  const uint32_t raw = st + pi * rowbytes;
+  const uint32_t rb = smem_u32(raw_bar);
+  if (ok) {
+    mbar_arrive_expect_tx(rb, rowbytes);
+    bulk_g2s(raw, p.kv + row * FP8_ROW, rowbytes, rb);
+  } else {
+    for (uint32_t j = 0; j < rowbytes; j += 16) st_shared_v4(raw + j, make_uint4(0, 0, 0, 0));
+    mbar_arrive(rb);
+  }
+  const float4 sc = ok ? __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4)) : make_float4(0, 0, 0, 0);
+  if (!wait_or_abort(c, raw_bar, raw_par)) return false;
+  // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them; rank 1:
+  // bytes 0..32767, blocks 4-7 lie past them
+  const int split = rope ? 5 : 4;
+  for (int kb = split; kb < 8; kb++)
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      uint4 lo, hi;
+      dequant16(ld_shared_v4(raw + kb * 64 + u * 16), kb < 4 ? (kb < 2 ? sc.x : sc.y) : (kb < 6 ? sc.z : sc.w), lo, hi);
+      st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
+      st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
+    }
+  if (rope)
+#pragma unroll
+    for (int j = 0; j < 8; j++) st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + 512 + j * 16));
+  uint4 v[20];  // e4m3 bytes of blocks 0 .. split-1 (at most 5 x 64 bytes)
+#pragma unroll
+  for (int u = 0; u < 20; u++)
+    if (u < split * 4) v[u] = ld_shared_v4(raw + u * 16);
+  named_bar_sync(kGatherBar, kGatherThreads);  // every staged byte below the blocks has been read
+#pragma unroll
+  for (int u = 0; u < 20; u++) {
+    if (u >= split * 4) break;
+    const int kb = u >> 2, ch = 2 * (u & 3);
+    uint4 lo, hi;
+    dequant16(v[u], kb < 2 ? sc.x : (kb < 4 ? sc.y : sc.z), lo, hi);
+    st_shared_v4(st + kb * kBlkBytes + pi * 128 + ((ch ^ sw) << 4), lo);
+    st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((ch + 1) ^ sw) << 4), hi);
+  }
+  return true;
 }
 
 // Thread pi (0..63) of the gather warps (0 and 3) owns key slot pi of every
@@ -373,9 +434,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format == MLA_KV_FP8_E4M3;
   const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
-  const int nblk = c.rank == 0 ? 9 : 8;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
-  const int sw = pi & 7;
   uint32_t g = 0, sq = 0;  // tiles; stages of the ring (rank 0: query stages too)
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
@@ -385,8 +444,9 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
       const int qrow = it.b * p.T * p.H + it.row0;
       for (int qh = 0; qh < q_stages(it); qh++, sq++) {
         const uint32_t s = sq % 3;
-        if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
-        if (!wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1)) return false;
+        bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1);
+        if (ok) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1);
+        if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;  // all 64 give up together
         const uint32_t bar = smem_u32(&br.kv_full[s]);
         if (pi == 0) {
           mbar_arrive_expect_tx(bar, kStage0Bytes);
@@ -395,6 +455,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
           mbar_arrive(bar);
         }
         mbar_arrive(smem_u32(&br.kv_full_b[s]));
+        mbar_arrive(smem_u32(&br.raw_full[s]));  // keeps the raw barrier's phase in step with the stage
       }
     }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
@@ -412,10 +473,12 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      if (!wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1)) return false;
-      if (c.rank == 0 && !wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1)) return false;
-      for (int kb = 0; kb < nblk; kb++)
-        gather_block(p, fp8, row, kb, kv0 + s * stage_bytes + kb * kBlkBytes + pi * 128, sw);
+      bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1);
+      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1);
+      // all 64 threads agree before the barriers inside the row copy
+      if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
+      ok = gather_row_to_stage(c, fp8, row, kv0 + s * stage_bytes, pi, c.rank == 0, &br.raw_full[s], (sq / 3) & 1);
+      if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
       if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
@@ -963,6 +1026,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
       mbar_init(smem_u32(&br.kv_empty[s]), 1);
       mbar_init(smem_u32(&br.kv_full_b[s]), kGather ? kGatherThreads : 1);
       mbar_init(smem_u32(&br.kv_empty_b[s]), 1);
+      mbar_init(smem_u32(&br.raw_full[s]), kGatherThreads);
     }
     for (int i = 0; i < kMaskRing; i++) mbar_init(smem_u32(&br.mfull[i]), kGather ? 2 : 1);
     for (int i = 0; i < P_RING; i++) {
