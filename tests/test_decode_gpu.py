@@ -163,3 +163,22 @@ def test_repeat_calls_identical(mla):
     a = G.run(w, dev=d)
     b = G.run(w, dev=d)
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+
+
+def test_output_only_16_byte_aligned(mla, oracle_mod):
+    """out 16 bytes past a 32-byte boundary: the epilogue must use its
+    16-byte stores there (32-byte stores need 32-byte alignment)."""
+    w = make_workload("align", 3, 1, 128, [700, 64, 130], seed=21)
+    d = G.to_device(w)
+    md, ns = mla.metadata(d["sk"], w.H, w.T)
+    n = w.B * w.T * w.H * 512
+    buf = torch.full((n + 8,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(w.B, w.T, w.H, 512)
+    assert out.data_ptr() % 32 == 16
+    o, lse = mla.decode(d["q"], d["kv"], d["bt"], d["sk"], softmax_scale=w.softmax_scale,
+                        tile_md=md, num_splits=ns, out=out)
+    torch.cuda.synchronize()
+    assert o.data_ptr() == out.data_ptr()
+    assert torch.all(buf[:8] == 7.0), "wrote before the output"
+    res = dict(out=o.float().cpu().numpy().astype(np.float64), lse=lse.cpu().numpy().astype(np.float64))
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
