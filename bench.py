@@ -89,7 +89,7 @@ def work_of(w, batches=None):
 
 
 class Clocks:
-    """nvidia-smi sampling (every 50 ms) around the timed region."""
+    """nvidia-smi sampling (every 10 ms) around the timed region."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -101,7 +101,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(index), "-lms", "50"],
+                 "-i", str(index), "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -236,6 +236,9 @@ def run_gpu(args, w, world, rank, local):
     import mla_decode_attention_05_gb300 as mla
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # nvidia-smi takes a moment to start sampling: start it before the
+    # inputs are uploaded so that it is running through the timed region
+    clocks = Clocks(local) if rank == 0 else None
     stream = torch.cuda.current_stream(dev)
     q_h = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
     if w.kv_format == workloads.KV_BF16:
@@ -290,7 +293,6 @@ def run_gpu(args, w, world, rank, local):
         e.record(stream)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     if clocks:
@@ -347,7 +349,7 @@ def run_gpu(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
