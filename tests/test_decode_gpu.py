@@ -78,6 +78,11 @@ SMALL = [
     dict(B=2, T=2, H=64, seqlens=[300, 200], topk=100, topk_pad_count=9, fp8=True),
     dict(B=2, T=1, H=128, seqlens=[400, 70], topk=64),
     dict(B=1, T=1, H=64, seqlens=[64], topk=1),
+    dict(B=2, T=1, H=1, seqlens=[300, 65]),
+    dict(B=2, T=8, H=16, seqlens=[200, 9], causal=True),
+    dict(B=1, T=16, H=32, seqlens=[700], causal=True),
+    dict(B=2, T=4, H=64, seqlens=[900, 260], topk=130, topk_pad_count=5),
+    dict(B=1, T=1, H=128, seqlens=[4160], fp8=True),
 ]
 
 
