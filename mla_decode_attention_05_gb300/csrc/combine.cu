@@ -10,6 +10,19 @@ namespace {
 
 constexpr int kWarps = 8;
 
+__device__ __forceinline__ void acc_add(float4 (&acc)[4], const float4 (&v)[4], float w) {
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    acc[k].x = fmaf(w, v[k].x, acc[k].x);
+    acc[k].y = fmaf(w, v[k].y, acc[k].y);
+    acc[k].z = fmaf(w, v[k].z, acc[k].z);
+    acc[k].w = fmaf(w, v[k].w, acc[k].w);
+  }
+}
+
+// Lane l of the warp of row r holds output values 4*(32k + l) .. +3, k < 4:
+// every 16-byte load and 8-byte store of the warp covers one contiguous
+// 512 / 256-byte span.  Two splits are loaded at a time.
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(DecodeParams p) {
   const int i = blockIdx.x;
@@ -22,37 +35,42 @@ combine_kernel(DecodeParams p) {
   if (r >= it.rows) return;
   float m = -INFINITY;
   for (int s = lane; s < ns; s += 32)
-    m = fmaxf(m, p.ws_lse[(size_t)(base + s) * M_TILE + r]);
+    m = fmaxf(m, __ldcg(p.ws_lse + (size_t)(base + s) * M_TILE + r));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float acc[16];
+  float4 acc[4];
 #pragma unroll
-  for (int k = 0; k < 16; k++) acc[k] = 0.f;
+  for (int k = 0; k < 4; k++) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < ns; s++) {
-      float ls = p.ws_lse[(size_t)(base + s) * M_TILE + r];
-      if (ls == -INFINITY) continue;
-      float w = exp2f(ls - m);
-      sum += w;
-      const float2 *src = reinterpret_cast<const float2 *>(
-          p.ws_o + ((size_t)(base + s) * M_TILE + r) * D_V);
+    for (int s = 0; s < ns; s += 2) {
+      const bool two = s + 1 < ns;  // every split slot holds a written partial
+      const float l0 = __ldcg(p.ws_lse + (size_t)(base + s) * M_TILE + r);
+      const float l1 = two ? __ldcg(p.ws_lse + (size_t)(base + s + 1) * M_TILE + r) : -INFINITY;
+      const float4 *src0 = reinterpret_cast<const float4 *>(p.ws_o + ((size_t)(base + s) * M_TILE + r) * D_V);
+      const float4 *src1 = src0 + (M_TILE * D_V) / 4;
+      float4 v0[4], v1[4];
 #pragma unroll
-      for (int k = 0; k < 8; k++) {
-        float2 v = src[lane + 32 * k];
-        acc[2 * k] = fmaf(w, v.x, acc[2 * k]);
-        acc[2 * k + 1] = fmaf(w, v.y, acc[2 * k + 1]);
-      }
+      for (int k = 0; k < 4; k++) v0[k] = __ldcg(src0 + 32 * k + lane);
+#pragma unroll
+      for (int k = 0; k < 4; k++) v1[k] = two ? __ldcg(src1 + 32 * k + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m);
+      const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m);
+      sum += w0 + w1;
+      acc_add(acc, v0, w0);
+      acc_add(acc, v1, w1);
     }
   }
   const int R = it.row0 + r;
   const int t = R / p.H, h = R % p.H;
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
-      p.out + (((size_t)it.b * p.T + t) * p.H + h) * D_V);
+  uint2 *dst = reinterpret_cast<uint2 *>(p.out + (((size_t)it.b * p.T + t) * p.H + h) * D_V);
 #pragma unroll
-  for (int k = 0; k < 8; k++)
-    dst[lane + 32 * k] = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+  for (int k = 0; k < 4; k++) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
+    dst[32 * k + lane] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+  }
   if (lane == 0)
     p.lse[((size_t)it.b * p.H + h) * p.T + t] = sum > 0.f ? (m + log2f(sum)) * LN2 : -INFINITY;
 }
