@@ -15,6 +15,11 @@ TFLOP/s counts 2*576 + 2*512 flops per (query row, valid key).
 --impl reference times the float64 CPU oracle on the host cores on a
 bounded, rotating sample of the same workload (one sequence per step, all
 heads) and reports the same metric.
+
+--op kv_insert times the cache producer instead (mla_kv_insert: RMSNorm of
+each new token's latent row, per-128 FP8 quantisation, paged write) on
+--tokens new tokens filling a cache of as many slots; `value` is its
+algorithmic GB/s (1160 bytes read and 656 written per token).
 """
 from __future__ import annotations
 
@@ -346,6 +351,145 @@ def run_gpu(args, w, world, rank, local):
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, launches=launches_per_step * K)
 
 
+# --- KV insert ------------------------------------------------------------------
+
+INSERT_METRIC = "MLA KV insert GB/s (RMSNorm + per-128 FP8 quantise + paged write); % of HBM roofline"
+INSERT_BYTES_PER_TOKEN = 1024 + 128 + 8 + 640 + 16  # latent + k_pe + slot read; FP8 row + 4 scales written
+
+
+def insert_workload(n_tokens: int):
+    """n_tokens new tokens, one per slot of a cache of exactly n_tokens slots
+    (64-token pages), FP8 rows with per-128 scales."""
+    pages = (n_tokens + 63) // 64
+    return workloads.make_insert_inputs(n_tokens, pages, 64, seed=4242, skip_every=0)
+
+
+def insert_cpu_baseline(inp, budget_s: float = 10.0):
+    from oracle import kv_insert as OK
+    kv = inp.qkv[:, workloads.KV_C_COL:]
+    pe = inp.qkv[:, workloads.K_PE_COL:]
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < budget_s and done < inp.N:
+        OK.insert_row(OK.FMT_FP8_TILE, kv[done, :512], pe[done, :64], inp.w_kva, inp.eps)
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": done * INSERT_BYTES_PER_TOKEN / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"tokens 0..{done - 1} of {inp.N} ({done} rows) in {dt:.1f} s, one row at a time"}
+
+
+def run_insert(args, world, rank, local, hbm, peak_src):
+    import ctypes
+    import torch
+    import mla_decode_attention_05_gb300 as mla
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    clocks = Clocks(local) if rank == 0 else None
+    inp = insert_workload(args.tokens)
+    N = inp.N
+    stream = torch.cuda.current_stream(dev)
+    qkv_h = torch.from_numpy(inp.qkv.view(np.int16)).view(torch.bfloat16)
+    qkv = qkv_h.to(dev)
+    w_kva = torch.from_numpy(inp.w_kva.view(np.int16)).view(torch.bfloat16).to(dev)
+    slots_h = torch.from_numpy(inp.slots)
+    slots = slots_h.to(dev)
+    cache = torch.zeros((inp.num_pages, 64, 640), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((inp.num_pages, 64, 4), dtype=torch.float32, device=dev)
+    L = mla.lib()
+    P = ctypes.c_void_p
+    sptr = P(stream.cuda_stream)
+    ld = qkv.stride(0)
+
+    def step(src, sl, ld_):
+        rc = L.mla_kv_insert(P(src.data_ptr() + 2 * workloads.KV_C_COL), ld_, P(src.data_ptr() + 2 * workloads.K_PE_COL),
+                             ld_, P(w_kva.data_ptr()), ctypes.c_float(inp.eps), P(sl.data_ptr()), N,
+                             P(cache.data_ptr()), mla.KV_FP8_E4M3, inp.num_pages, 64, P(scales.data_ptr()),
+                             None, sptr)
+        if rc != 0:
+            raise RuntimeError(L.mla_last_error_string().decode())
+
+    for _ in range(args.warmup):
+        step(qkv, slots, ld)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
+    for i in range(K):
+        evs[i].record(stream)
+        step(qkv, slots, ld)
+    evs[K].record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    total_ms = evs[0].elapsed_time(evs[K])
+    status = mla.device_status()
+    clk = clocks.finish() if clocks else None
+
+    # end to end: the token rows (latent + k_pe, 1152 bytes) and slots from
+    # pinned host memory, the insert, the written cache and scales back
+    rows_h = torch.cat([qkv_h[:, workloads.KV_C_COL:workloads.KV_C_COL + 512],
+                        qkv_h[:, workloads.K_PE_COL:workloads.K_PE_COL + 64]], dim=1).contiguous().pin_memory()
+    sl_pin = slots_h.pin_memory()
+    rows_d = torch.empty_like(rows_h, device=dev)
+    sl_d = torch.empty_like(sl_pin, device=dev)
+    cache_h = torch.empty(cache.shape, dtype=cache.dtype).pin_memory()
+    scales_h = torch.empty(scales.shape, dtype=scales.dtype).pin_memory()
+
+    def e2e_step():
+        rows_d.copy_(rows_h, non_blocking=True)
+        sl_d.copy_(sl_pin, non_blocking=True)
+        rc = L.mla_kv_insert(P(rows_d.data_ptr()), 576, P(rows_d.data_ptr() + 1024), 576, P(w_kva.data_ptr()),
+                             ctypes.c_float(inp.eps), P(sl_d.data_ptr()), N, P(cache.data_ptr()),
+                             mla.KV_FP8_E4M3, inp.num_pages, 64, P(scales.data_ptr()), None, sptr)
+        if rc != 0:
+            raise RuntimeError(L.mla_last_error_string().decode())
+        cache_h.copy_(cache, non_blocking=True)
+        scales_h.copy_(scales, non_blocking=True)
+
+    Ke = max(3, min(K, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / Ke, world)
+    step_ms = max_over_ranks(total_ms / K, world)
+    kern_ms = max_over_ranks(statistics.mean(per), world)
+    if rank != 0:
+        return
+    nbytes = N * INSERT_BYTES_PER_TOKEN + 1024
+    k_gbs = nbytes / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": INSERT_METRIC, "value": world * nbytes / (step_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
+        "tokens_per_s": world * N / (step_ms * 1e-3),
+        "config": {"workload": f"kv_insert_fp8_tile_n{N}", "tokens": N, "page_size": 64,
+                   "num_pages": inp.num_pages, "bytes_per_token": INSERT_BYTES_PER_TOKEN,
+                   "l2": f"{N * INSERT_BYTES_PER_TOKEN / 1e6:.0f} MB touched per step vs {L2_BYTES / 1e6:.0f} MB L2; no flush",
+                   "parallelism": f"weak, {world} independent replica(s)"},
+        "roofline": {"bound": "hbm", "achieved": k_gbs, "peak": hbm, "unit": "GB/s", "frac": k_gbs / hbm,
+                     "traffic": None, "kernel_ms": kern_ms,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": rows_h.numel() * 2 + sl_pin.numel() * 8,
+                "d2h_bytes_per_step": cache.numel() + scales.numel() * 4},
+        "gpu_launches": K, "device_status": status, "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = insert_cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -357,10 +501,30 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first BATCH sequences of the workload (same values; "
                          "used for small profiling cases)")
+    ap.add_argument("--op", default="decode", choices=["decode", "kv_insert"],
+                    help="decode: the attention path (default); kv_insert: the cache producer")
+    ap.add_argument("--tokens", type=int, default=262144, help="new tokens per kv_insert step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
+
+    if args.op == "kv_insert":
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            inp = insert_workload(args.tokens)
+            cb = insert_cpu_baseline(inp, budget_s=min(60.0, 0.5 * (args.steps + args.warmup)))
+            print(json.dumps({"impl": "reference", "metric": INSERT_METRIC, "value": cb["value"], "unit": "GB/s",
+                              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                              "data": "synthetic", "config": {"workload": f"kv_insert_fp8_tile_n{inp.N}"},
+                              "cpu_baseline": cb,
+                              "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        run_insert(args, world, rank, local, hbm, peak_src)
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -211,6 +211,57 @@ int mla_decode_noalloc(const void *q, const void *kv_cache, int kv_format,
                        void *out, float *lse, int B, int T, int H,
                        mla_stream_t stream);
 
+/*
+ * KV insert: the producer of the cache this library reads (vLLM kimi_k3
+ * specialized-decode "mla.query" page, MlaQuery.insert: RMSNorm of the
+ * latent KV row, then the write of that row and k_pe into its cache slot).
+ * For each new token j with slot = slots[j] >= 0 (slot = page * page_size +
+ * offset; -1 = skip):
+ *   x      = the 512 latent values of row j (bf16, at kv_c + j * ld_kv)
+ *   S      = sum(x_i^2), exact, rounded once to fp32
+ *   mean   = fp32(fp32(S / 512) + eps)
+ *   r      = fp32(1 / fp32(sqrt(mean)))  (0 if mean == 0)
+ *   n_i    = bf16(fp32(fp32(x_i * w_kva[i]) * r))
+ *            (fp32 steps and the bf16 rounding: IEEE, to nearest even)
+ *   pe     = the 64 RoPE'd key values of row j (bf16, at k_pe + j * ld_pe)
+ * and writes the cache row cache[page][offset] as
+ *   MLA_KV_BF16:             n_0..n_511, pe_0..pe_63 (bf16, 1152 bytes)
+ *   MLA_KV_FP8_E4M3:         per 128-value tile t: s_t = fp32(max|n| / 448)
+ *                            (1 when the tile is all zeros) into
+ *                            kv_scales[page][offset][t],
+ *                            e4m3(fp32(n_i * fp32(1 / s_t)));
+ *                            then pe as bf16 (640 bytes: the decode's FP8
+ *                            rows, value = e4m3 * scale)
+ *   MLA_KV_FP8_E4M3_TENSOR:  e4m3(fp32(n_i * k_scale_inv)), e4m3(fp32(pe_i *
+ *                            k_scale_inv)) (576 bytes; the per-tensor
+ *                            FP8 layout; written only, mla_decode does not
+ *                            read it)
+ * e4m3 = OCP FP8 E4M3, round to nearest even, saturated to +-448.  The sum
+ * of squares is taken as integers (a bf16 square is an 8-bit integer squared
+ * times a power of two), so the written bytes are a function of the inputs
+ * alone, independent of the order of additions.  Inputs must be finite.
+ * Slots must be distinct (two tokens writing one slot race).
+ *
+ *   kv_c, ld_kv   device bf16 rows, latent at columns 0..511, row stride ld_kv
+ *                 elements (>= 512, multiple of 8; e.g. a fused qkv row with
+ *                 kv_c = qkv + 1536 and ld_kv = 2112)
+ *   k_pe, ld_pe   device bf16 rows, RoPE'd key at columns 0..63 (ld_pe >= 64,
+ *                 multiple of 8)
+ *   w_kva         device bf16 [512] RMSNorm weight;  eps >= 0
+ *   slots         device int64 [N]
+ *   kv_cache      device [num_pages][page_size][row bytes] of the format
+ *   kv_scales     MLA_KV_FP8_E4M3: device fp32 [num_pages][page_size][4]
+ *                 (written); otherwise unused
+ *   k_scale_inv   MLA_KV_FP8_E4M3_TENSOR: device fp32 scalar; otherwise unused
+ * All pointers 16-byte aligned (slots 8).  Asynchronous on stream.  A slot
+ * outside [0, num_pages * page_size) other than -1 is skipped and sets
+ * MLA_STATUS_BAD_PAGE.  Returns MLA_OK or a negative MLA_ERR_* code.
+ */
+#define MLA_KV_FP8_E4M3_TENSOR 2
+int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, const void *w_kva, float eps,
+                  const int64_t *slots, int N, void *kv_cache, int kv_format, int num_pages, int page_size,
+                  float *kv_scales, const float *k_scale_inv, mla_stream_t stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *mla_last_error_string(void);
 

@@ -12,6 +12,8 @@ every call raises.
     out, lse = mla.decode(q, kv_cache, block_table, cache_seqlens,
                           softmax_scale=192 ** -0.5,
                           tile_md=tile_md, num_splits=num_splits)
+    mla.kv_insert(kv_c, k_pe, w_kva, slots, kv_cache, eps=1e-6,
+                  kv_scales=kv_scales)   # the cache producer
 """
 from __future__ import annotations
 
@@ -27,6 +29,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmla_decode.so")
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_FP8_E4M3_TENSOR = 2
 PAGE_SIZE = 64
 D_QK = 576
 D_V = 512
@@ -67,6 +70,7 @@ def lib():
                                      P, P, i, P, sz, P, P, i, i, i, P]
             L.mla_decode_noalloc.argtypes = [P, P, i, i, i, P, i, P, P, i, P, ctypes.c_float, i,
                                              P, P, i, i, i, P]
+            L.mla_kv_insert.argtypes = [P, i, P, i, P, ctypes.c_float, P, i, P, i, i, i, P, P, P]
             L.mla_last_error_string.restype = ctypes.c_char_p
             L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.mla_profile_events.argtypes = [P, P]
@@ -229,6 +233,65 @@ def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.T
             block_table.shape[1], _ptr(cache_seqlens), _ptr(topk_indices), topk, _ptr(kv_scales),
             float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
     return out, lse
+
+
+_INSERT_ROW = {KV_BF16: 1152, KV_FP8_E4M3: FP8_ROW_BYTES, KV_FP8_E4M3_TENSOR: D_QK}
+
+
+def _rows_view(t: torch.Tensor, name: str, width: int):
+    """A bf16 matrix whose rows may be strided (a column slice of a wider
+    row, e.g. the latent part of a fused projection) -> (tensor, ld)."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    if t.dim() != 2 or t.shape[1] < width or t.stride(1) != 1:
+        raise ValueError(f"{name} must be [N, >={width}] with unit column stride")
+    return t, t.stride(0) if t.shape[0] > 1 else max(t.shape[1], width)
+
+
+def kv_insert(kv_c: torch.Tensor, k_pe: torch.Tensor, w_kva: torch.Tensor, slots: torch.Tensor,
+              kv_cache: torch.Tensor, *, eps: float, kv_scales: Optional[torch.Tensor] = None,
+              k_scale_inv: Optional[torch.Tensor] = None, fp8_per_tensor: bool = False):
+    """RMSNorm the new tokens' latent rows and write them, with k_pe, into
+    their cache slots, on the current stream (mla_kv_insert).
+
+    kv_c bf16 [N, >=512] (columns 0..511 are read; rows may be a strided
+    column slice); k_pe bf16 [N, >=64]; w_kva bf16 [512]; slots int64 [N]
+    (-1 = skip).  kv_cache: bf16 [P, page, 576] (bf16 rows), uint8
+    [P, page, 640] with kv_scales fp32 [P, page, 4] (the decode's FP8 rows),
+    or uint8 [P, page, 576] with fp8_per_tensor=True and k_scale_inv fp32 [1].
+    Returns kv_cache."""
+    kv_c, ld_kv = _rows_view(kv_c, "kv_c", D_V)
+    k_pe, ld_pe = _rows_view(k_pe, "k_pe", 64)
+    dev = kv_c.device
+    N = kv_c.shape[0]
+    if k_pe.shape[0] != N:
+        raise ValueError("kv_c / k_pe row counts differ")
+    _need(w_kva, "w_kva", torch.bfloat16, dev, 1)
+    _need(slots, "slots", torch.int64, dev, 1)
+    if slots.shape[0] != N or w_kva.shape[0] != D_V:
+        raise ValueError("slots must be [N], w_kva [512]")
+    _need(kv_cache, "kv_cache", kv_cache.dtype, dev, 3)
+    if kv_cache.dtype == torch.bfloat16:
+        fmt = KV_BF16
+    elif kv_cache.dtype == torch.uint8:
+        fmt = KV_FP8_E4M3_TENSOR if fp8_per_tensor else KV_FP8_E4M3
+    else:
+        raise TypeError("kv_cache must be bfloat16 or uint8")
+    if kv_cache.shape[2] * kv_cache.element_size() != _INSERT_ROW[fmt]:
+        raise ValueError(f"kv_cache rows must be {_INSERT_ROW[fmt]} bytes for this format")
+    if fmt == KV_FP8_E4M3:
+        _need(kv_scales, "kv_scales", torch.float32, dev, 3)
+        if tuple(kv_scales.shape) != (kv_cache.shape[0], kv_cache.shape[1], 4):
+            raise ValueError("kv_scales must be [P, page, 4]")
+    if fmt == KV_FP8_E4M3_TENSOR:
+        _need(k_scale_inv, "k_scale_inv", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(lib().mla_kv_insert(
+            _ptr(kv_c), ld_kv, _ptr(k_pe), ld_pe, _ptr(w_kva), float(eps), _ptr(slots), N,
+            _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1],
+            _ptr(kv_scales) if fmt == KV_FP8_E4M3 else None,
+            _ptr(k_scale_inv) if fmt == KV_FP8_E4M3_TENSOR else None, _stream(dev)))
+    return kv_cache
 
 
 def device_status() -> int:

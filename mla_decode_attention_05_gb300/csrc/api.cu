@@ -233,6 +233,50 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   return ok();
 }
 
+int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, const void *w_kva, float eps,
+                  const int64_t *slots, int N, void *kv_cache, int kv_format, int num_pages, int page_size,
+                  float *kv_scales, const float *k_scale_inv, mla_stream_t stream) {
+  if (N < 0) return fail(MLA_ERR_INVALID_ARG, "N = %d must be >= 0", N);
+  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_E4M3 && kv_format != MLA_KV_FP8_E4M3_TENSOR)
+    return fail(MLA_ERR_INVALID_ARG, "kv_format %d unknown", kv_format);
+  if (num_pages < 1 || page_size < 1)
+    return fail(MLA_ERR_INVALID_ARG, "num_pages = %d, page_size = %d must be >= 1", num_pages, page_size);
+  if (ld_kv < mla::D_V || ld_kv % 8) return fail(MLA_ERR_INVALID_ARG, "ld_kv = %d: need >= 512, multiple of 8", ld_kv);
+  if (ld_pe < mla::D_ROPE || ld_pe % 8)
+    return fail(MLA_ERR_INVALID_ARG, "ld_pe = %d: need >= 64, multiple of 8", ld_pe);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(MLA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (N == 0) return ok();
+  if (!kv_c || !k_pe || !w_kva || !slots || !kv_cache) return fail(MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(w_kva, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slots, 8))
+    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe, w_kva, kv_cache must be 16-byte aligned, slots 8");
+  if (kv_format == MLA_KV_FP8_E4M3 && (!kv_scales || !aligned(kv_scales, 16)))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scales must be a 16-byte aligned pointer for MLA_KV_FP8_E4M3");
+  if (kv_format == MLA_KV_FP8_E4M3_TENSOR && (!k_scale_inv || !aligned(k_scale_inv, 4)))
+    return fail(MLA_ERR_INVALID_ARG, "k_scale_inv must be a 4-byte aligned pointer for MLA_KV_FP8_E4M3_TENSOR");
+  unsigned int *st = nullptr;
+  int rc;
+  if ((rc = status_ptr(&st)) != MLA_OK) return rc;
+  mla::KvInsertParams p{};
+  p.kv_c = static_cast<const __nv_bfloat16 *>(kv_c);
+  p.k_pe = static_cast<const __nv_bfloat16 *>(k_pe);
+  p.w_kva = static_cast<const __nv_bfloat16 *>(w_kva);
+  p.slots = slots;
+  p.cache = static_cast<uint8_t *>(kv_cache);
+  p.kv_scales = kv_scales;
+  p.k_scale_inv = k_scale_inv;
+  p.status = st;
+  p.n_slots = (long long)num_pages * page_size;
+  p.ld_kv = ld_kv;
+  p.ld_pe = ld_pe;
+  p.N = N;
+  p.kv_format = kv_format;
+  p.eps = eps;
+  cudaError_t e = mla::launch_kv_insert(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kv insert launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 const char *mla_last_error_string(void) { return g_err; }
 
 int mla_device_status(uint32_t *status) {

@@ -139,5 +139,23 @@ cudaError_t launch_metadata(const int32_t *seqlens, int B, int H, int T,
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream,
                           cudaEvent_t ev_before, cudaEvent_t ev_after);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream);
+
+// One KV insert call (mla_kv_insert), by value.
+struct KvInsertParams {
+  const __nv_bfloat16 *kv_c;  // latent rows, stride ld_kv elements
+  const __nv_bfloat16 *k_pe;  // RoPE rows, stride ld_pe elements
+  const __nv_bfloat16 *w_kva;
+  const int64_t *slots;
+  uint8_t *cache;
+  float *kv_scales;
+  const float *k_scale_inv;
+  unsigned int *status;
+  long long n_slots;  // num_pages * page_size
+  int ld_kv, ld_pe;
+  int N;
+  int kv_format;
+  float eps;
+};
+cudaError_t launch_kv_insert(const KvInsertParams &p, cudaStream_t stream);
 void set_last_error(const char *msg);
 }  // namespace mla

@@ -76,6 +76,30 @@ def test_argument_checks(L, args, code):
     assert len(L.mla_last_error_string()) > 0
 
 
+@pytest.mark.parametrize("args,code", [
+    (dict(N=-1), -1), (dict(kv_format=3), -1), (dict(num_pages=0), -1), (dict(page_size=0), -1),
+    (dict(ld_kv=500), -1), (dict(ld_kv=516), -1), (dict(ld_pe=60), -1), (dict(eps=-1.0), -1),
+    (dict(eps=float("nan")), -1), (dict(kv_c=0), -1), (dict(kv_c=264), -1), (dict(slots=260), -1),
+    (dict(kv_format=1, scales=None), -1), (dict(kv_format=1, scales=264), -1),
+    (dict(kv_format=2, ksi=None), -1), (dict(kv_format=2, ksi=258), -1),
+    (dict(N=0, kv_c=0, slots=0, kv=0), 0),
+])
+def test_kv_insert_argument_checks(L, args, code):
+    """mla_kv_insert rejects each bad argument before any CUDA call; N = 0 is
+    a valid empty call that launches nothing."""
+    base = dict(kv_c=256, ld_kv=2112, k_pe=256, ld_pe=2112, w=256, eps=1e-6, slots=256, N=4,
+                kv=256, kv_format=0, num_pages=4, page_size=64, scales=256, ksi=256)
+    base.update(args)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = L.mla_kv_insert(v(base["kv_c"]), base["ld_kv"], v(base["k_pe"]), base["ld_pe"], v(base["w"]),
+                         ctypes.c_float(base["eps"]), v(base["slots"]), base["N"], v(base["kv"]),
+                         base["kv_format"], base["num_pages"], base["page_size"], v(base["scales"]),
+                         v(base["ksi"]), None)
+    assert rc == code
+    if code:
+        assert len(L.mla_last_error_string()) > 0
+
+
 def test_library_missing_fails_loudly(tmp_path, monkeypatch):
     """No silent fallback: without the built library every call raises."""
     import mla_decode_attention_05_gb300 as m

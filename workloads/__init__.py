@@ -312,6 +312,63 @@ def config(i: int) -> Workload:
     raise ValueError(i)
 
 
+# --- KV insert inputs ---------------------------------------------------------
+
+QKV_COLS = 2112     # fused projection row: q_a (1536) | latent KV (512) | k_pe (64)
+KV_C_COL = 1536
+K_PE_COL = 2048
+
+
+@dataclasses.dataclass
+class InsertInputs:
+    qkv: np.ndarray      # uint16 bf16 bits [N, 2112]
+    w_kva: np.ndarray    # uint16 bf16 bits [512]
+    slots: np.ndarray    # int64 [N], -1 = skip
+    num_pages: int
+    page_size: int
+    eps: float
+    k_scale_inv: float
+
+    @property
+    def N(self) -> int:
+        return self.qkv.shape[0]
+
+
+def make_insert_inputs(N: int, num_pages: int, page_size: int = PAGE, *, seed: int,
+                       skip_every: int = 9, eps: float = 1e-6,
+                       k_scale_inv: float = 0.75) -> InsertInputs:
+    """New-token rows for the cache insert, laid out like the fused projection
+    output the insert reads (latent KV at columns 1536..2047, k_pe at
+    2048..2111).  Each token's latent row has its own scale (log-uniform over
+    2^-6 .. 2^3) so the normalisation matters; w_kva ~ 1 + 0.25 N(0,1).  Slots
+    are distinct, drawn without replacement from the whole cache, with every
+    ``skip_every``-th token set to -1.  When N >= 4 the first rows are special
+    cases: row 0 all zeros, row 1 one large outlier, row 2 with its second
+    128-value tile all zeros, row 3 constant."""
+    g = _Rng(seed)
+    scale = np.exp2(g.uniform(-6.0, 3.0, N)).astype(np.float32)
+    lat = _bf16_normal(g, (N, D_V), std=1.0)
+    lat_f = (lat.astype(np.uint32) << 16).view(np.float32) * scale[:, None]
+    lat = _round_bf16_bits(np.ascontiguousarray(lat_f, dtype=np.float32))
+    if N >= 4:
+        lat[0] = 0
+        lat[1, 77] = _round_bf16_bits(np.array([300.0], np.float32))[0]
+        lat[2, 128:256] = 0
+        lat[3] = _round_bf16_bits(np.full(D_V, -0.3125, np.float32))
+    qkv_bits = _bf16_normal(g, (N, QKV_COLS), std=1.0)
+    qkv_bits[:, KV_C_COL:KV_C_COL + D_V] = lat
+    w = 1.0 + 0.25 * g.normal_f32(D_V, 1.0)
+    w_bits = _round_bf16_bits(np.ascontiguousarray(w, dtype=np.float32))
+    total = num_pages * page_size
+    if N > total:
+        raise ValueError("more tokens than cache slots")
+    slots = g.permutation(total)[:N].astype(np.int64)
+    if skip_every > 0:
+        slots[skip_every - 1::skip_every] = -1
+    return InsertInputs(qkv=qkv_bits, w_kva=w_bits, slots=slots, num_pages=num_pages,
+                        page_size=page_size, eps=float(eps), k_scale_inv=float(k_scale_inv))
+
+
 def kv_bytes_per_token(kv_format: int) -> int:
     """Algorithmic bytes of one valid key: 576 bf16, or 512 e4m3 + 4 fp32
     scales + 64 bf16 RoPE."""
