@@ -226,8 +226,8 @@ int mla_decode_noalloc(const void *q, const void *kv_cache, int kv_format,
  *   pe     = the 64 RoPE'd key values of row j (bf16, at k_pe + j * ld_pe)
  * and writes the cache row cache[page][offset] as
  *   MLA_KV_BF16:             n_0..n_511, pe_0..pe_63 (bf16, 1152 bytes)
- *   MLA_KV_FP8_E4M3:         per 128-value tile t: s_t = fp32(max|n| / 448)
- *                            (1 when the tile is all zeros) into
+ *   MLA_KV_FP8_E4M3:         per 128-value tile t: s_t = fp32(max|n| / 448),
+ *                            at least 2^-126 (1 when the tile is all zeros), into
  *                            kv_scales[page][offset][t],
  *                            e4m3(fp32(n_i * fp32(1 / s_t)));
  *                            then pe as bf16 (640 bytes: the decode's FP8

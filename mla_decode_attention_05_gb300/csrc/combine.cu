@@ -25,6 +25,7 @@ __device__ __forceinline__ void acc_add(float4 (&acc)[4], const float4 (&v)[4], 
 // 512 / 256-byte span.  Two splits are loaded at a time.
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(DecodeParams p) {
+  grid_dep_wait();  // the decode kernel's partials are complete
   const int i = blockIdx.x;
   const int base = p.num_splits[i];
   const int ns = p.num_splits[i + 1] - base;
@@ -78,9 +79,20 @@ combine_kernel(DecodeParams p) {
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream) {
-  dim3 grid(p.n_items, M_TILE / kWarps);
-  combine_kernel<<<grid, kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the decode kernel: its blocks
+  // are scheduled while the decode kernel runs and wait for it in
+  // grid_dep_wait()
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_items, M_TILE / kWarps);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 }  // namespace mla

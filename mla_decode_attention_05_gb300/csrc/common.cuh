@@ -128,6 +128,15 @@ __device__ inline float e4m3_to_float(uint32_t c) {
   return __uint_as_float(__float_as_uint(v) | s);
 }
 
+// Programmatic dependent launch (griddepcontrol): a kernel launched with the
+// programmatic-serialization attribute may begin while the kernel before it
+// in the stream is still running.  grid_dep_wait() blocks until that kernel
+// has completed and its memory operations are visible (a no-op for a kernel
+// launched without the attribute), so it comes before the first read of any
+// input; grid_dep_trigger() lets the next such kernel begin launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace mla
 
 // Host-side launchers (one per translation unit).

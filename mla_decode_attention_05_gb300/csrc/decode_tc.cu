@@ -1058,6 +1058,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote arrive or copy
   const uint32_t tmem = br.tmem_base;
+  // Everything above overlaps the kernel before this one (the schedule);
+  // no input is read before this point.
+  grid_dep_wait();
+  grid_dep_trigger();
 
   if (kGather) {
     if (warp == 0 || warp == 3) producer_gather(c, &q_map, warp == 0 ? lane : 32 + lane);
@@ -1150,10 +1154,21 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
   auto kern = gather ? decode_tc_kernel<true> : decode_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(2 * p.num_parts);
   if (ev_before) cudaEventRecord(ev_before, stream);
-  kern<<<grid, threads_of(gather), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  e = cudaGetLastError();
+  // A programmatic dependent of the previous kernel of the stream (normally
+  // the schedule): set-up runs while that kernel finishes, inputs are read
+  // after grid_dep_wait().
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.num_parts);
+  cfg.blockDim = dim3(threads_of(gather));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
   if (ev_after) cudaEventRecord(ev_after, stream);
   return e;
 }

@@ -14,9 +14,13 @@
 // accumulator aligned to the largest one, so the sum does not depend on the
 // order of additions and every code below is a function of the inputs.
 //
-// One warp per token.  Lane l holds latent values 16l .. 16l + 15, so the
-// 8 lanes 8t .. 8t+7 hold FP8 scale tile t (values 128t .. 128t + 127) and
-// every lane stores one 16-byte piece of the latent part of the row.
+// One warp per token, a persistent grid of warps striding over the tokens.
+// Each warp keeps its next kStages - 1 tokens (latent row, k_pe, slot) in
+// flight into a ring in shared memory with cp.async while it processes the
+// current one.
+// Lane l holds latent values 16l .. 16l + 15, so the 8 lanes 8t .. 8t+7 hold
+// FP8 scale tile t (values 128t .. 128t + 127) and every lane stores one
+// 16-byte piece of the latent part of the row.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -25,6 +29,7 @@ namespace mla {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kBlocksPerSm = 3;
 
 template <int N>
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[N], int at) {
@@ -36,52 +41,74 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[N], int at) {
   }
 }
 
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  const uint32_t ca = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t cb = __nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t cc = __nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t cd = __nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3);
-  return ca | (cb << 8) | (cc << 16) | (cd << 24);
+// Two values -> two e4m3 codes (first value in the low byte), saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// The 16 bf16 values of this lane: value = m * 2^(ee - 134) with m the
-// 8-bit significand (hidden bit included) and ee the biased exponent (1 for
-// subnormals).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
+// v << s with the PTX rule for large shifts: an amount of 32 or more (a
+// negative s reads as a large unsigned amount) gives 0.
+__device__ __forceinline__ uint32_t shl_or_zero(uint32_t v, int s) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
+
+// A bf16 value is m * 2^(ee - 134): m the 8-bit significand (hidden bit
+// included), ee the biased exponent (1 for subnormals).
 __device__ __forceinline__ void split_bf16(uint32_t h, uint32_t &m, int &ee) {
   const int e = (h >> 7) & 0xFF;
   m = (h & 0x7Fu) | (e ? 0x80u : 0u);
   ee = e ? e : 1;
 }
 
-// Position of the largest square in the accumulator: 512 squares below 2^16
-// each, placed at bit 102 at most, stay below 2^127.
-constexpr int kAccTop = 102;
+// The 16 bf16 values of a lane, two per word (the first in the low half).
+struct Row16 {
+  uint32_t w[8];
+};
 
-// sum of the squares of the warp's 512 bf16 values (finite), rounded once
-// to fp32 (ties to even).
-__device__ float exact_sum_sq_rn(const uint32_t (&xw)[8]) {
-  int emax = 0;
-#pragma unroll
-  for (int i = 0; i < 16; i++) {
-    uint32_t m;
-    int ee;
-    split_bf16((xw[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu, m, ee);
-    if (m) emax = max(emax, ee);
-  }
-  emax = (int)__reduce_max_sync(0xffffffffu, (unsigned)emax);
-  if (emax == 0) return 0.f;  // all zeros
+__device__ __forceinline__ uint32_t half_of(const Row16 &xw, int i) {
+  return (xw.w[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
+}
+
+// acc * 2^e0 (acc < 2^127; sticky: the true value lies strictly above acc,
+// by less than one unit of acc's lowest bit) rounded to fp32, ties to even.
+__device__ float round_to_f32(unsigned __int128 acc, int e0, bool sticky) {
+  if (sticky) acc |= 1u;
+  const uint64_t hi = (uint64_t)(acc >> 64);
+  const int lead = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)(uint64_t)acc);
+  const int q = max(lead - 23, -149 - e0);  // position of the fp32 quantum in acc
+  if (q <= 0) return ldexpf((float)(uint32_t)acc, e0);  // exact: acc < 2^24
+  if (q >= lead + 2) return 0.f;                         // below half the smallest subnormal
+  unsigned __int128 keep = acc >> q;
+  const unsigned __int128 rem = acc & (((unsigned __int128)1 << q) - 1);
+  const unsigned __int128 half = (unsigned __int128)1 << (q - 1);
+  if (rem > half || (rem == half && (keep & 1))) keep += 1;
+  return ldexpf((float)(uint32_t)keep, q + e0);  // keep <= 2^24: exact; overflow -> inf
+}
+
+// Wide form of the sum of squares, for rows whose values span more than
+// 2^31: squares placed relative to the largest one at bit 102 (512 squares
+// below 2^16 stay below 2^127); those that fall below bit 0 leave their
+// remainder as a sticky bit.
+__device__ __noinline__ float sum_sq_wide(const Row16 xw, int emax) {
+  constexpr int kTop = 102;
   unsigned __int128 acc = 0;
   bool sticky = false;
 #pragma unroll
   for (int i = 0; i < 16; i++) {
     uint32_t m;
     int ee;
-    split_bf16((xw[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu, m, ee);
+    split_bf16(half_of(xw, i), m, ee);
     const uint32_t t = m * m;
-    const int sh = kAccTop - 2 * (emax - ee);
+    const int sh = kTop - 2 * (emax - ee);
     if (sh >= 0) {
       acc += (unsigned __int128)t << sh;
-    } else if (sh > -32) {  // below the accumulator: keep what fits, note the rest
+    } else if (sh > -32) {
       acc += t >> -sh;
       sticky |= (t & ((1u << -sh) - 1u)) != 0u;
     } else {
@@ -94,75 +121,134 @@ __device__ float exact_sum_sq_rn(const uint32_t (&xw)[8]) {
     const uint64_t hi = __shfl_xor_sync(0xffffffffu, (unsigned long long)(acc >> 64), o);
     acc += ((unsigned __int128)hi << 64) | lo;
   }
-  // A nonzero remainder far below the rounding position only matters as a
-  // sticky bit.
-  if (__any_sync(0xffffffffu, sticky)) acc |= 1u;
-  // S = acc * 2^e0; round acc to 24 significant bits (or to the fp32
-  // subnormal quantum 2^-149)
-  const int e0 = 2 * emax - 268 - kAccTop;
-  const uint64_t hi = (uint64_t)(acc >> 64);
-  const int lead = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)(uint64_t)acc);
-  const int q = max(lead - 23, -149 - e0);
-  if (q <= 0) return ldexpf((float)(uint32_t)acc, e0);  // exact: acc < 2^24
-  if (q >= lead + 2) return 0.f;                         // below half the smallest subnormal
-  unsigned __int128 keep = acc >> q;
-  const unsigned __int128 rem = acc & (((unsigned __int128)1 << q) - 1);
-  const unsigned __int128 half = (unsigned __int128)1 << (q - 1);
-  if (rem > half || (rem == half && (keep & 1))) keep += 1;
-  return ldexpf((float)(uint32_t)keep, q + e0);  // keep <= 2^24: exact; overflow -> inf
+  return round_to_f32(acc, 2 * emax - 268 - kTop, __any_sync(0xffffffffu, sticky));
 }
 
-__global__ void __launch_bounds__(kWarps * 32) kv_insert_kernel(KvInsertParams p) {
-  const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (j >= p.N) return;
-  const long long slot = p.slots[j];
+// Sum of the squares of the warp's 512 bf16 values (finite), exact, rounded
+// once to fp32.  A square is m^2 * 2^(2 ee - 268); relative to the largest
+// exponent emax it sits at bit s = 2 (ee - emax) + 31.  Squares with
+// s in [0, 31] go to `hi` at bit s, those with s in [-32, -1] to `lo` at bit
+// s + 32 (each sum stays below 2^56), so hi * 2^32 + lo is the exact sum in
+// units of 2^(2 emax - 331).
+//   Fast form: when emax >= 32 every zero lands below bit -32 of the window
+// and adds nothing, so every value can take the normal significand
+// 0x80 | mantissa.  A row with a nonzero value below the window (its
+// exponent under emax - 31: subnormals included) or with emax < 32 takes
+// the wide form.  emax and the smallest nonzero magnitude come from the
+// 15-bit magnitude patterns, which order like the values.
+__device__ __forceinline__ float sum_sq_rn(const Row16 &xw) {
+  uint32_t amax = 0, amin = 0x7FFFu;
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const uint32_t a0 = xw.w[k] & 0x7FFFu, a1 = (xw.w[k] >> 16) & 0x7FFFu;
+    amax = max(amax, max(a0, a1));
+    amin = min(amin, min(a0 ? a0 : 0x7FFFu, a1 ? a1 : 0x7FFFu));
+  }
+  amax = __reduce_max_sync(0xffffffffu, amax);
+  if (amax == 0) return 0.f;  // all zeros
+  amin = __reduce_min_sync(0xffffffffu, amin);
+  const int emax = (int)(amax >> 7);
+  if (emax < 32 || (int)(amin >> 7) < emax - 31) return sum_sq_wide(xw, max(emax, 1));
+  const int base = 31 - 2 * emax;
+  uint64_t hi = 0, lo = 0;
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    const uint32_t h = half_of(xw, i);
+    const uint32_t m = (h & 0x7Fu) | 0x80u;
+    const uint32_t t = m * m;
+    const int s = 2 * (int)((h >> 7) & 0xFFu) + base;
+    hi += (uint64_t)t * shl_or_zero(1u, s);
+    lo += (uint64_t)t * shl_or_zero(1u, s + 32);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    hi += __shfl_xor_sync(0xffffffffu, (unsigned long long)hi, o);
+    lo += __shfl_xor_sync(0xffffffffu, (unsigned long long)lo, o);
+  }
+  return round_to_f32(((unsigned __int128)hi << 32) + lo, 2 * emax - 331, false);
+}
+
+constexpr int kStages = 4;
+constexpr int kStageBytes = 1024 + 128 + 16;  // latent row, k_pe, slot (8 bytes, padded)
+constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Start the copies of token j into a stage (nothing past the last token);
+// every call commits one group, so the group count per stage stays fixed.
+__device__ __forceinline__ void issue_token(const KvInsertParams &p, int j, int lane, uint32_t stage) {
+  if (j < p.N) {
+    const uint8_t *x = reinterpret_cast<const uint8_t *>(p.kv_c + (size_t)j * p.ld_kv) + 32 * lane;
+    cp_async16(stage + 32 * lane, x);
+    cp_async16(stage + 32 * lane + 16, x + 16);
+    if (lane < 8) cp_async16(stage + 1024 + 16 * lane, p.k_pe + (size_t)j * p.ld_pe + 8 * lane);
+    if (lane == 0) cp_async8(stage + 1152, p.slots + j);
+  }
+  cp_async_commit();
+}
+
+struct Token {
+  uint4 xa, xb, pe;
+  long long slot;
+};
+
+__device__ __forceinline__ void insert_token(const KvInsertParams &p, const Token &tk, const float (&w)[16],
+                                             int lane) {
+  const long long slot = tk.slot;
   if (slot < 0 || slot >= p.n_slots) {
     if (slot != -1 && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
     return;
   }
-  const uint4 *xr = reinterpret_cast<const uint4 *>(p.kv_c + (size_t)j * p.ld_kv) + 2 * lane;
-  const uint4 *wr = reinterpret_cast<const uint4 *>(p.w_kva) + 2 * lane;
-  const uint4 xa = __ldg(xr), xb = __ldg(xr + 1);
-  uint4 pe = make_uint4(0u, 0u, 0u, 0u);
-  if (lane < 8) pe = __ldg(reinterpret_cast<const uint4 *>(p.k_pe + (size_t)j * p.ld_pe) + lane);
-  float x[16], w[16];
-  unpack8(xa, x, 0);
-  unpack8(xb, x, 8);
-  unpack8(__ldg(wr), w, 0);
-  unpack8(__ldg(wr + 1), w, 8);
-
-  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-  const float S = exact_sum_sq_rn(xw);
+  const Row16 xr = {{tk.xa.x, tk.xa.y, tk.xa.z, tk.xa.w, tk.xb.x, tk.xb.y, tk.xb.z, tk.xb.w}};
+  const uint32_t *xw = xr.w;
+  const float S = sum_sq_rn(xr);
   const float mean = __fadd_rn(__fmul_rn(S, 1.f / 512.f), p.eps);
   const float r = mean > 0.f ? __fdiv_rn(1.f, __fsqrt_rn(mean)) : 0.f;
 
+  // n_i = bf16(fp32(fp32(x_i * w_i) * r)), kept as packed bf16 pairs
+  uint32_t nb[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const float x0 = __uint_as_float(xw[k] << 16), x1 = __uint_as_float(xw[k] & 0xFFFF0000u);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__fmul_rn(x0, w[2 * k]), r),
+                                              __fmul_rn(__fmul_rn(x1, w[2 * k + 1]), r));
+    nb[k] = *reinterpret_cast<uint32_t *>(&b2);
+  }
+
+  if (p.kv_format == MLA_KV_BF16) {
+    uint8_t *row = p.cache + (size_t)slot * (D_QK * 2);
+    uint4 *dst = reinterpret_cast<uint4 *>(row) + 2 * lane;
+    dst[0] = make_uint4(nb[0], nb[1], nb[2], nb[3]);
+    dst[1] = make_uint4(nb[4], nb[5], nb[6], nb[7]);
+    if (lane < 8) reinterpret_cast<uint4 *>(row + D_V * 2)[lane] = tk.pe;
+    return;
+  }
   float n[16];
 #pragma unroll
-  for (int i = 0; i < 16; i++)
-    n[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x[i], w[i]), r)));
-
-  uint8_t *row;
-  if (p.kv_format == MLA_KV_BF16) {
-    row = p.cache + (size_t)slot * (D_QK * 2);
-    uint32_t h[8];
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(n[2 * k], n[2 * k + 1]);  // exact: n is bf16
-      h[k] = *reinterpret_cast<uint32_t *>(&b2);
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(row) + 2 * lane;
-    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-    if (lane < 8) reinterpret_cast<uint4 *>(row + D_V * 2)[lane] = pe;
-  } else if (p.kv_format == MLA_KV_FP8_E4M3) {
-    row = p.cache + (size_t)slot * FP8_ROW;
+  for (int k = 0; k < 8; k++) {
+    n[2 * k] = __uint_as_float(nb[k] << 16);
+    n[2 * k + 1] = __uint_as_float(nb[k] & 0xFFFF0000u);
+  }
+  if (p.kv_format == MLA_KV_FP8_E4M3) {
+    uint8_t *row = p.cache + (size_t)slot * FP8_ROW;
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(n[i]));
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    // s = fp32(amax / 448), at least the smallest normal 2^-126 (so 1 / s
+    // stays finite); 1 for an all-zero tile
+    const float sc = amax > 0.f ? fmaxf(__fdiv_rn(amax, 448.f), 0x1p-126f) : 1.f;
     const float inv = __fdiv_rn(1.f, sc);
     uint32_t c[4];
 #pragma unroll
@@ -170,13 +256,13 @@ __global__ void __launch_bounds__(kWarps * 32) kv_insert_kernel(KvInsertParams p
       c[k] = e4m3x4(__fmul_rn(n[4 * k], inv), __fmul_rn(n[4 * k + 1], inv), __fmul_rn(n[4 * k + 2], inv),
                     __fmul_rn(n[4 * k + 3], inv));
     reinterpret_cast<uint4 *>(row)[lane] = make_uint4(c[0], c[1], c[2], c[3]);
-    if (lane < 8) reinterpret_cast<uint4 *>(row + D_V)[lane] = pe;
+    if (lane < 8) reinterpret_cast<uint4 *>(row + D_V)[lane] = tk.pe;
     const float s1 = __shfl_sync(0xffffffffu, sc, 8);
     const float s2 = __shfl_sync(0xffffffffu, sc, 16);
     const float s3 = __shfl_sync(0xffffffffu, sc, 24);
     if (lane == 0) reinterpret_cast<float4 *>(p.kv_scales)[slot] = make_float4(sc, s1, s2, s3);
   } else {  // MLA_KV_FP8_E4M3_TENSOR
-    row = p.cache + (size_t)slot * D_QK;
+    uint8_t *row = p.cache + (size_t)slot * D_QK;
     const float ksi = __ldg(p.k_scale_inv);
     uint32_t c[4];
 #pragma unroll
@@ -186,7 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32) kv_insert_kernel(KvInsertParams p
     reinterpret_cast<uint4 *>(row)[lane] = make_uint4(c[0], c[1], c[2], c[3]);
     if (lane < 8) {
       float f[8];
-      unpack8(pe, f, 0);
+      unpack8(tk.pe, f, 0);
       reinterpret_cast<uint2 *>(row + D_V)[lane] =
           make_uint2(e4m3x4(__fmul_rn(f[0], ksi), __fmul_rn(f[1], ksi), __fmul_rn(f[2], ksi), __fmul_rn(f[3], ksi)),
                      e4m3x4(__fmul_rn(f[4], ksi), __fmul_rn(f[5], ksi), __fmul_rn(f[6], ksi), __fmul_rn(f[7], ksi)));
@@ -194,11 +280,50 @@ __global__ void __launch_bounds__(kWarps * 32) kv_insert_kernel(KvInsertParams p
   }
 }
 
+__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) kv_insert_kernel(KvInsertParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int first = blockIdx.x * kWarps + warp;
+  const int stride = gridDim.x * kWarps;
+  if (first >= p.N) return;
+  uint8_t *ring = smem + warp * kStages * kStageBytes;
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  float w[16];
+  const uint4 *wr = reinterpret_cast<const uint4 *>(p.w_kva) + 2 * lane;
+  unpack8(__ldg(wr), w, 0);
+  unpack8(__ldg(wr + 1), w, 8);
+#pragma unroll
+  for (int s = 0; s < kStages - 1; s++) issue_token(p, first + s * stride, lane, ring_s + s * kStageBytes);
+  int st = 0;
+  for (int j = first; j < p.N; j += stride) {
+    const int ahead = st == 0 ? kStages - 1 : st - 1;  // the stage freed last iteration
+    issue_token(p, j + (kStages - 1) * stride, lane, ring_s + ahead * kStageBytes);
+    cp_async_wait<kStages - 1>();  // this token's group has landed (for this lane's copies)
+    __syncwarp();                  // ... and lane 0's slot copy is visible to all lanes
+    const uint8_t *cur = ring + st * kStageBytes;
+    Token tk;
+    tk.xa = *reinterpret_cast<const uint4 *>(cur + 32 * lane);
+    tk.xb = *reinterpret_cast<const uint4 *>(cur + 32 * lane + 16);
+    tk.pe = lane < 8 ? *reinterpret_cast<const uint4 *>(cur + 1024 + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
+    tk.slot = *reinterpret_cast<const long long *>(cur + 1152);
+    __syncwarp();  // every lane has read the stage before it is refilled
+    insert_token(p, tk, w, lane);
+    st = st + 1 == kStages ? 0 : st + 1;
+  }
+  cp_async_wait<0>();
+}
+
 }  // namespace
 
 cudaError_t launch_kv_insert(const KvInsertParams &p, cudaStream_t stream) {
-  const int blocks = (p.N + kWarps - 1) / kWarps;
-  kv_insert_kernel<<<blocks, kWarps * 32, 0, stream>>>(p);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int need = (p.N + kWarps - 1) / kWarps;
+  const int blocks = need < sms * kBlocksPerSm ? need : sms * kBlocksPerSm;
+  static_assert(kSmemBytes <= 48 * 1024, "dynamic shared memory above the default limit");
+  kv_insert_kernel<<<blocks, kWarps * 32, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

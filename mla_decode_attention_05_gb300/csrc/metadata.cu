@@ -54,6 +54,7 @@ metadata_kernel(const int32_t *seqlens, int H, int T, int topk, int causal,
   __shared__ int warp_sums[32];
   __shared__ int carry;
   const int tid = threadIdx.x;
+  grid_dep_trigger();  // the decode kernel may set itself up meanwhile
   if (tid == 0) { carry = 0; C[0] = 0; }
   __syncthreads();
   // 1. cost line: C[i+1] = C[i] + FIXED_COST + n_i

@@ -15,9 +15,9 @@ numpy; every step after S is one IEEE fp32 operation, ties to even):
   n_i  = bf16(fp32(fp32(x_i * w_i) * r))
 Formats:
   bf16         n (512 bf16) then k_pe (64 bf16)
-  fp8 (tile)   per 128-value tile t: s_t = fp32(max|n| / 448) (1 for an
-               all-zero tile), e4m3(fp32(n_i * fp32(1 / s_t))); then k_pe as
-               bf16; scales [page][offset][4]
+  fp8 (tile)   per 128-value tile t: s_t = max(fp32(max|n| / 448), 2^-126)
+               (1 for an all-zero tile), e4m3(fp32(n_i * fp32(1 / s_t)));
+               then k_pe as bf16; scales [page][offset][4]
   fp8 (tensor) e4m3(fp32(n_i * ksi)), e4m3(fp32(pe_i * ksi))
 
 The encoders below (exact rational -> fp32, float -> bf16, float -> OCP FP8
@@ -165,7 +165,7 @@ def insert_row(fmt: int, x_bits, pe_bits, w_bits, eps: float, ksi: float = 1.0):
         for t in range(4):
             tile = n[128 * t:128 * (t + 1)]
             amax = np.float32(np.max(np.abs(tile)))
-            s_t = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+            s_t = max(np.float32(amax / np.float32(E4M3_MAX)), np.float32(2.0 ** -126)) if amax > 0 else np.float32(1.0)
             scales[t] = s_t
             inv = np.float32(1.0) / s_t
             q = (f32(tile) * inv).astype(np.float64)  # float32 product, correctly rounded

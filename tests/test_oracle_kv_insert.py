@@ -234,13 +234,34 @@ def test_fp8_tile_scales_codes_and_error_bound():
         if not tile.any():
             assert sc[t] == 1.0 and not row[128 * t:128 * (t + 1)].any()
             continue
-        assert sc[t] == np.float32(np.float32(np.abs(tile).max()) / np.float32(448))
+        assert sc[t] == max(np.float32(np.float32(np.abs(tile).max()) / np.float32(448)), np.float32(2.0 ** -126))
         vals = K.e4m3_bits_to_f64(row[128 * t:128 * (t + 1)])
         assert np.abs(vals).max() == 448.0
         d = deq[128 * t:128 * (t + 1)]
         # 3 mantissa bits: half an ulp is 2^-4 relative (normals), 2^-10 * s below 2^-6 * s
         assert np.all(np.abs(d - tile) <= np.maximum(2.0 ** -4 * np.abs(tile), 2.0 ** -10 * sc[t]) * (1 + 1e-6))
     np.testing.assert_array_equal(row[512:].view("<u2"), pe)
+
+
+def test_extreme_rows_stay_finite_and_follow_the_limits():
+    """The generator's edge rows: a 2^172 span (tile scales down to the
+    smallest normal), a sum of squares beyond fp32 (r = 0: zeros), a row of
+    bf16 subnormals (the sum underflows: r = 1 / sqrt(eps))."""
+    inp = W.make_insert_inputs(8, 1, seed=3)
+    lat = inp.qkv[:, W.KV_C_COL:W.KV_C_COL + 512]
+    pe = inp.qkv[:, W.K_PE_COL:W.K_PE_COL + 64]
+    for r in (4, 5, 6):
+        row, sc = K.insert_row(K.FMT_FP8_TILE, lat[r], pe[r], inp.w_kva, inp.eps)
+        assert np.all((row[:512] & 0x7F) != 0x7F), r  # no NaN code
+        assert np.all(np.isfinite(sc)) and np.all(sc >= 2.0 ** -126), r
+    assert np.isinf(K.fraction_to_f32(K.exact_sum_sq(bf16_val(lat[5]))))
+    assert not bf16_val(K.rms_norm_row(lat[5], inp.w_kva, inp.eps)).any()  # +-0
+    assert K.fraction_to_f32(K.exact_sum_sq(bf16_val(lat[6]))) == 0
+    n6 = bf16_val(K.rms_norm_row(lat[6], ONES, inp.eps))
+    r6 = np.float32(1) / np.sqrt(np.float32(inp.eps))
+    np.testing.assert_array_equal(n6, bf16_val(bf16((bf16_val(lat[6]).astype(np.float32) * r6).astype(np.float64))))
+    _, sc4 = K.insert_row(K.FMT_FP8_TILE, lat[4], pe[4], inp.w_kva, inp.eps)
+    assert sc4[3] == np.float32(2.0 ** -126)
 
 
 def test_fp8_tensor_codes_with_unit_and_power_of_two_scale():

@@ -344,7 +344,9 @@ def make_insert_inputs(N: int, num_pages: int, page_size: int = PAGE, *, seed: i
     are distinct, drawn without replacement from the whole cache, with every
     ``skip_every``-th token set to -1.  When N >= 4 the first rows are special
     cases: row 0 all zeros, row 1 one large outlier, row 2 with its second
-    128-value tile all zeros, row 3 constant."""
+    128-value tile all zeros, row 3 constant; when N >= 8 also row 4 spanning
+    2^40 down to bf16 subnormals, row 5 with a sum of squares beyond fp32
+    (2^60 values) and row 6 of bf16 subnormals only."""
     g = _Rng(seed)
     scale = np.exp2(g.uniform(-6.0, 3.0, N)).astype(np.float32)
     lat = _bf16_normal(g, (N, D_V), std=1.0)
@@ -355,6 +357,14 @@ def make_insert_inputs(N: int, num_pages: int, page_size: int = PAGE, *, seed: i
         lat[1, 77] = _round_bf16_bits(np.array([300.0], np.float32))[0]
         lat[2, 128:256] = 0
         lat[3] = _round_bf16_bits(np.full(D_V, -0.3125, np.float32))
+    if N >= 8:
+        # row 4: values from 2^40 down to bf16 subnormals (a span beyond 2^31)
+        span = np.exp2(np.linspace(40.0, -132.0, D_V)).astype(np.float32)
+        lat[4] = _round_bf16_bits(span * np.where(np.arange(D_V) % 3 == 0, -1, 1).astype(np.float32))
+        # row 5: squares whose sum overflows fp32 (2^60 squared, 512 times)
+        lat[5] = _round_bf16_bits(np.full(D_V, 2.0 ** 60, np.float32) * np.where(np.arange(D_V) % 2, -1, 1).astype(np.float32))
+        # row 6: bf16 subnormals only (the sum underflows fp32)
+        lat[6] = (np.arange(D_V) % 127 + 1).astype(np.uint16)
     qkv_bits = _bf16_normal(g, (N, QKV_COLS), std=1.0)
     qkv_bits[:, KV_C_COL:KV_C_COL + D_V] = lat
     w = 1.0 + 0.25 * g.normal_f32(D_V, 1.0)
