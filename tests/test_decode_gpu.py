@@ -121,6 +121,36 @@ def test_many_splits_combine(mla, oracle_mod):
     G.compare_rows(w, res, G.all_rows(w), oracle_mod)
 
 
+def test_schedule_reused_by_consecutive_calls(mla, oracle_mod):
+    """One schedule serves several decode calls in stream order (as one
+    schedule serves every layer of a step), with identical results."""
+    w = make_workload("reuse", 3, 1, 128, [3000, 700, 5000], seed=21)
+    d = G.to_device(w)
+    md, ns = mla.metadata(d["sk"], w.H, w.T, num_parts=24)
+    outs = []
+    for _ in range(3):
+        out, lse = mla.decode(d["q"], d["kv"], d["bt"], d["sk"], softmax_scale=w.softmax_scale,
+                              tile_md=md, num_splits=ns)
+        outs.append((out.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert np.diff(ns.cpu().numpy()).max() > 1
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    res = dict(out=outs[0][0].float().cpu().numpy().astype(np.float64),
+               lse=outs[0][1].cpu().numpy().astype(np.float64))
+    G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
+
+
+def test_more_workers_than_fit_at_once(mla, oracle_mod):
+    """num_parts above the worker pairs the device holds at once: later
+    workers start as earlier ones finish; items whose pieces span both
+    groups still combine correctly."""
+    w = make_workload("waves", 2, 1, 64, [9000, 7000], seed=22)
+    res = G.run(w, num_parts=120)
+    assert mla.device_status() == 0
+    G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
+
+
 def test_metadata_bit_exact(mla):
     """Device schedule == the plain-Python statement of the rule."""
     from oracle import schedule as S
