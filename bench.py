@@ -20,6 +20,10 @@ heads) and reports the same metric.
 each new token's latent row, per-128 FP8 quantisation, paged write) on
 --tokens new tokens filling a cache of as many slots; `value` is its
 algorithmic GB/s (1160 bytes read and 656 written per token).
+
+--op query_absorb times the query path (mla_query_absorb: q_a RMSNorm, Q_B,
+W_UK) for --tokens tokens (default 64) and 128 heads, with L2 flushed before
+each call; `value` is GB/s of weights + q_a + q bytes.
 """
 from __future__ import annotations
 
@@ -497,6 +501,124 @@ def run_insert(args, world, rank, local, hbm, peak_src):
     print(json.dumps(line), flush=True)
 
 
+# --- query absorption --------------------------------------------------------------
+
+QUERY_METRIC = "MLA query absorption GB/s (q_a RMSNorm + Q_B + W_UK, B=64 tokens, H=128); % of HBM roofline"
+
+
+def query_bytes(N: int, H: int) -> int:
+    """Algorithmic bytes of one call: the two weight matrices, w_qa, the q_a
+    rows read and the query rows written."""
+    return H * 192 * 1536 * 2 + H * 128 * 512 * 2 + 1536 * 2 + N * 1536 * 2 + N * H * 576 * 2
+
+
+def query_cpu_baseline(inp, budget_s: float = 10.0):
+    from oracle import query_absorb as OQ
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < budget_s and done < inp.N:
+        OQ.query_absorb(inp.qkv[done:done + 1], inp.w_qa, inp.eps, inp.w_qb, inp.w_uk)
+        done += 1
+    dt = time.perf_counter() - t0
+    per_token = query_bytes(1, inp.H)
+    return {"value": done * per_token / dt / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"tokens 0..{done - 1} of {inp.N}, one call per token (all weights each), {dt:.1f} s, float64"}
+
+
+def run_query(args, world, rank, local, hbm, peak_src):
+    import ctypes
+    import torch
+    import mla_decode_attention_05_gb300 as mla
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    clocks = Clocks(local) if rank == 0 else None
+    N, H = args.tokens, 128
+    inp = workloads.make_query_inputs(N, H, seed=4343)
+    stream = torch.cuda.current_stream(dev)
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    qkv_h = t16(inp.qkv)
+    qkv = qkv_h.to(dev)
+    w_qa, w_qb, w_uk = (t16(a).to(dev) for a in (inp.w_qa, inp.w_qb, inp.w_uk))
+    q = torch.empty((N, H, 576), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mla.query_absorb_workspace_bytes(N, H), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2: weights come from HBM
+    L = mla.lib()
+    P = ctypes.c_void_p
+    sptr = P(stream.cuda_stream)
+
+    def step(src, ld, out):
+        rc = L.mla_query_absorb(P(src.data_ptr()), ld, P(w_qa.data_ptr()), ctypes.c_float(inp.eps),
+                                P(w_qb.data_ptr()), P(w_uk.data_ptr()), N, H, P(out.data_ptr()), P(ws.data_ptr()),
+                                ws.numel(), sptr)
+        if rc != 0:
+            raise RuntimeError(L.mla_last_error_string().decode())
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(qkv, qkv.stride(0), q)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(qkv, qkv.stride(0), q)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    per = [a.elapsed_time(b) for a, b in ev]
+    status = mla.device_status()
+    clk = clocks.finish() if clocks else None
+
+    # end to end: q_a rows from pinned host memory, the call, q back
+    qa_h = qkv_h[:, :1536].contiguous().pin_memory()
+    qa_d = torch.empty_like(qa_h, device=dev)
+    q_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    Ke = max(3, min(K, 20))
+    times = []
+    for i in range(Ke + 2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        qa_d.copy_(qa_h, non_blocking=True)
+        step(qa_d, 1536, q)
+        q_h.copy_(q, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    step_ms = max_over_ranks(statistics.mean(per), world)
+    e2e_ms = max_over_ranks(statistics.mean(times), world)
+    if rank != 0:
+        return
+    nbytes = query_bytes(N, H)
+    gbs = nbytes / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": QUERY_METRIC, "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights of the layer's shapes)",
+        "config": {"workload": f"query_absorb_n{N}_h{H}", "tokens": N, "H": H, "bytes": nbytes,
+                   "l2": "256 MB written before every timed call (weights 92 MB would otherwise stay in L2)",
+                   "gemms": "cuBLAS (bf16, fp32 accumulate): Q_B and the per-head W_UK",
+                   "parallelism": f"weak, {world} independent replica(s)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "kernel_ms": step_ms,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": qa_h.numel() * 2, "d2h_bytes_per_step": q_h.numel() * 2},
+        "gpu_launches": 2 * K, "device_status": status, "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = query_cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,14 +630,34 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first BATCH sequences of the workload (same values; "
                          "used for small profiling cases)")
-    ap.add_argument("--op", default="decode", choices=["decode", "kv_insert"],
-                    help="decode: the attention path (default); kv_insert: the cache producer")
-    ap.add_argument("--tokens", type=int, default=262144, help="new tokens per kv_insert step")
+    ap.add_argument("--op", default="decode", choices=["decode", "kv_insert", "query_absorb"],
+                    help="decode: the attention path (default); kv_insert: the cache producer; "
+                         "query_absorb: the query rows from q_a")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="new tokens per step (kv_insert: 262144; query_absorb: 64)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
 
+    if args.tokens is None:
+        args.tokens = 64 if args.op == "query_absorb" else 262144
+    if args.op == "query_absorb":
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            inp = workloads.make_query_inputs(args.tokens, 128, seed=4343)
+            cb = query_cpu_baseline(inp, budget_s=min(60.0, 1.0 * (args.steps + args.warmup)))
+            print(json.dumps({"impl": "reference", "metric": QUERY_METRIC, "value": cb["value"], "unit": "GB/s",
+                              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                              "data": "synthetic", "config": {"workload": f"query_absorb_n{inp.N}_h128"},
+                              "cpu_baseline": cb,
+                              "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        run_query(args, world, rank, local, hbm, peak_src)
+        return
     if args.op == "kv_insert":
         if args.impl == "reference":
             if rank != 0:

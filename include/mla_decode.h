@@ -262,6 +262,41 @@ int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, cons
                   const int64_t *slots, int N, void *kv_cache, int kv_format, int num_pages, int page_size,
                   float *kv_scales, const float *k_scale_inv, mla_stream_t stream);
 
+/*
+ * Query absorption: the query rows `q` that mla_decode reads, from the query
+ * part of the fused projection output (vLLM kimi_k3 specialized-decode
+ * "mla.query" page, MlaQuery.kernel: q_a RMSNorm, Q_B, W_UK).  For each of
+ * the N tokens (N = B * T; token n = b * T + t):
+ *   x     = the 1536 q_a values of row n (bf16, at q_a + n * ld_qa)
+ *   S     = sum(x_i^2), exact, rounded once to fp32
+ *   mean  = fp32(fp32(S / 1536) + eps);  r = fp32(1 / fp32(sqrt(mean))) (0 if mean == 0)
+ *   xq_i  = bf16(fp32(fp32(x_i * w_qa[i]) * r))
+ *   qb[h][p] = bf16(sum_k w_qb[h * 192 + p][k] * xq_k)     p < 192
+ *   q[n][h][l]       = bf16(sum_{p<128} qb[h][p] * w_uk[h][p][l])   l < 512
+ *   q[n][h][512 + i] = qb[h][128 + i]                               i < 64
+ * The sums of products accumulate in fp32 (cuBLAS GEMMs, loaded with dlopen
+ * at the first call); the RMSNorm is exact as stated.
+ *
+ *   q_a, ld_qa  device bf16 rows, q_a values at columns 0..1535, row stride
+ *               ld_qa elements (>= 1536, multiple of 8; the fused row:
+ *               ld_qa = 2112)
+ *   w_qa        device bf16 [1536];  eps >= 0
+ *   w_qb        device bf16 [H * 192][1536] (row h * 192 + p: head h, row p;
+ *               rows 0..127 no-PE, 128..191 RoPE)
+ *   w_uk        device bf16 [H][128][512]
+ *   q           device bf16 [N][H][576], written
+ *   workspace   device, >= mla_query_absorb_workspace_bytes(N, H), 256-byte
+ *               aligned: xq bf16 [N][1536] at 0, then qb bf16 [N][H * 192] at
+ *               the next multiple of 256 bytes (both left there)
+ * All other pointers 16-byte aligned.  Asynchronous on `stream`.  Returns
+ * MLA_OK, or MLA_ERR_UNSUPPORTED when cuBLAS cannot be loaded, or another
+ * negative MLA_ERR_* code.
+ */
+size_t mla_query_absorb_workspace_bytes(int N, int H);
+int mla_query_absorb(const void *q_a, int ld_qa, const void *w_qa, float eps, const void *w_qb,
+                     const void *w_uk, int N, int H, void *q, void *workspace, size_t workspace_bytes,
+                     mla_stream_t stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *mla_last_error_string(void);
 

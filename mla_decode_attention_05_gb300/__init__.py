@@ -71,6 +71,9 @@ def lib():
             L.mla_decode_noalloc.argtypes = [P, P, i, i, i, P, i, P, P, i, P, ctypes.c_float, i,
                                              P, P, i, i, i, P]
             L.mla_kv_insert.argtypes = [P, i, P, i, P, ctypes.c_float, P, i, P, i, i, i, P, P, P]
+            L.mla_query_absorb_workspace_bytes.argtypes = [i, i]
+            L.mla_query_absorb_workspace_bytes.restype = sz
+            L.mla_query_absorb.argtypes = [P, i, P, ctypes.c_float, P, P, i, i, P, P, sz, P]
             L.mla_last_error_string.restype = ctypes.c_char_p
             L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.mla_profile_events.argtypes = [P, P]
@@ -292,6 +295,52 @@ def kv_insert(kv_c: torch.Tensor, k_pe: torch.Tensor, w_kva: torch.Tensor, slots
             _ptr(kv_scales) if fmt == KV_FP8_E4M3 else None,
             _ptr(k_scale_inv) if fmt == KV_FP8_E4M3_TENSOR else None, _stream(dev)))
     return kv_cache
+
+
+D_QA = 1536
+QB_ROWS = 192
+
+
+def query_absorb_workspace_bytes(N: int, H: int) -> int:
+    n = lib().mla_query_absorb_workspace_bytes(N, H)
+    if n == 0:
+        raise MlaError(-1, "bad sizes for the query-absorption workspace")
+    return int(n)
+
+
+def query_absorb(q_a: torch.Tensor, w_qa: torch.Tensor, w_qb: torch.Tensor, w_uk: torch.Tensor, *,
+                 eps: float, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The decode's query rows from q_a, on the current stream
+    (mla_query_absorb): RMSNorm(q_a) x w_qa -> Q_B (192 rows per head) ->
+    W_UK on the 128 no-PE rows; returns q bf16 [N, H, 576] (reshape to
+    [B, T, H, 576] for decode()).
+
+    q_a bf16 [N, >=1536] (rows may be a strided column slice of the fused
+    projection output); w_qa bf16 [1536]; w_qb bf16 [H*192, 1536]; w_uk bf16
+    [H, 128, 512].  A caller-given workspace (uint8, >=
+    query_absorb_workspace_bytes(N, H)) keeps xq and qb for inspection."""
+    q_a, ld = _rows_view(q_a, "q_a", D_QA)
+    dev = q_a.device
+    N = q_a.shape[0]
+    _need(w_qa, "w_qa", torch.bfloat16, dev, 1)
+    _need(w_qb, "w_qb", torch.bfloat16, dev, 2)
+    _need(w_uk, "w_uk", torch.bfloat16, dev, 3)
+    H = w_uk.shape[0]
+    if w_qa.shape[0] != D_QA or tuple(w_qb.shape) != (H * QB_ROWS, D_QA) or tuple(w_uk.shape[1:]) != (128, D_V):
+        raise ValueError("expected w_qa [1536], w_qb [H*192, 1536], w_uk [H, 128, 512]")
+    if out is None:
+        out = torch.empty((N, H, D_QK), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev, 3)
+    if tuple(out.shape) != (N, H, D_QK):
+        raise ValueError("out must be [N, H, 576]")
+    need = query_absorb_workspace_bytes(N, H)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().mla_query_absorb(_ptr(q_a), ld, _ptr(w_qa), float(eps), _ptr(w_qb), _ptr(w_uk), N, H,
+                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream(dev)))
+    return out
 
 
 def device_status() -> int:

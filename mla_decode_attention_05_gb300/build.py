@@ -75,7 +75,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
     tmp = SO + f".tmp{os.getpid()}"
-    subprocess.check_call([nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"])
+    subprocess.check_call([nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl"])
     os.replace(tmp, SO)
     return SO
 

@@ -100,6 +100,33 @@ def test_kv_insert_argument_checks(L, args, code):
         assert len(L.mla_last_error_string()) > 0
 
 
+@pytest.mark.parametrize("args,code", [
+    (dict(N=-1), -1), (dict(H=0), -1), (dict(H=129), -1), (dict(ld=1535), -1), (dict(ld=1540), -1),
+    (dict(eps=-1.0), -1), (dict(eps=float("inf")), -1), (dict(q_a=0), -1), (dict(w_qb=264), -1),
+    (dict(ws=272), -1), (dict(ws_bytes=64), -3), (dict(N=0, q_a=0, ws=0), 0),
+])
+def test_query_absorb_argument_checks(L, args, code):
+    """mla_query_absorb rejects each bad argument before any CUDA or cuBLAS
+    call; N = 0 is a valid empty call."""
+    base = dict(q_a=256, ld=2112, w_qa=256, eps=1e-6, w_qb=256, w_uk=256, N=4, H=128, q=256, ws=512,
+                ws_bytes=1 << 30)
+    base.update(args)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    rc = L.mla_query_absorb(v(base["q_a"]), base["ld"], v(base["w_qa"]), ctypes.c_float(base["eps"]),
+                            v(base["w_qb"]), v(base["w_uk"]), base["N"], base["H"], v(base["q"]), v(base["ws"]),
+                            base["ws_bytes"], None)
+    assert rc == code
+    if code:
+        assert len(L.mla_last_error_string()) > 0
+
+
+def test_query_absorb_workspace_size(L):
+    import mla_decode_attention_05_gb300 as m
+    n = m.query_absorb_workspace_bytes(64, 128)
+    assert n >= 64 * 1536 * 2 + 64 * 128 * 192 * 2
+    assert L.mla_query_absorb_workspace_bytes(-1, 128) == 0 and L.mla_query_absorb_workspace_bytes(4, 0) == 0
+
+
 def test_library_missing_fails_loudly(tmp_path, monkeypatch):
     """No silent fallback: without the built library every call raises."""
     import mla_decode_attention_05_gb300 as m

@@ -379,6 +379,43 @@ def make_insert_inputs(N: int, num_pages: int, page_size: int = PAGE, *, seed: i
                         page_size=page_size, eps=float(eps), k_scale_inv=float(k_scale_inv))
 
 
+# --- query-absorption inputs ---------------------------------------------------
+
+@dataclasses.dataclass
+class QueryInputs:
+    qkv: np.ndarray      # uint16 bf16 bits [N, 2112]; q_a at columns 0..1535
+    w_qa: np.ndarray     # uint16 bf16 bits [1536]
+    w_qb: np.ndarray     # uint16 bf16 bits [H*192, 1536]
+    w_uk: np.ndarray     # uint16 bf16 bits [H, 128, 512]
+    eps: float
+
+    @property
+    def N(self) -> int:
+        return self.qkv.shape[0]
+
+    @property
+    def H(self) -> int:
+        return self.w_uk.shape[0]
+
+
+def make_query_inputs(N: int, H: int, *, seed: int, eps: float = 1e-6) -> QueryInputs:
+    """Synthetic inputs of the query path: fused projection rows whose q_a part
+    (columns 0..1535) has a per-token scale log-uniform over 2^-6 .. 2^3;
+    w_qa ~ 1 + 0.25 N(0,1); W_QB ~ N(0,1)/sqrt(1536) and W_UK ~ N(0,1)/sqrt(128)
+    (random weights of the layer's shapes: 192 Q_B rows per head, 128 of them
+    no-PE, and a 128 x 512 W_UK per head), all rounded to bf16."""
+    g = _Rng(seed)
+    scale = np.exp2(g.uniform(-6.0, 3.0, N)).astype(np.float32)
+    qa = _bf16_normal(g, (N, 1536), std=1.0)
+    qa_f = (qa.astype(np.uint32) << 16).view(np.float32) * scale[:, None]
+    qkv = _bf16_normal(g, (N, QKV_COLS), std=1.0)
+    qkv[:, :1536] = _round_bf16_bits(np.ascontiguousarray(qa_f, dtype=np.float32))
+    w_qa = _round_bf16_bits(np.ascontiguousarray(1.0 + 0.25 * g.normal_f32(1536, 1.0), dtype=np.float32))
+    w_qb = _bf16_normal(g, (H * 192, 1536), std=1.0 / math.sqrt(1536.0))
+    w_uk = _bf16_normal(g, (H, 128, 512), std=1.0 / math.sqrt(128.0))
+    return QueryInputs(qkv=qkv, w_qa=w_qa, w_qb=w_qb, w_uk=w_uk, eps=float(eps))
+
+
 def kv_bytes_per_token(kv_format: int) -> int:
     """Algorithmic bytes of one valid key: 576 bf16, or 512 e4m3 + 4 fp32
     scales + 64 bf16 RoPE."""
