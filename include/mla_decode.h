@@ -274,8 +274,10 @@ int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, cons
  *   qb[h][p] = bf16(sum_k w_qb[h * 192 + p][k] * xq_k)     p < 192
  *   q[n][h][l]       = bf16(sum_{p<128} qb[h][p] * w_uk[h][p][l])   l < 512
  *   q[n][h][512 + i] = qb[h][128 + i]                               i < 64
- * The sums of products accumulate in fp32 (cuBLAS GEMMs, loaded with dlopen
- * at the first call); the RMSNorm is exact as stated.
+ * The sums of products accumulate in fp32 (Q_B: a cuBLAS GEMM, loaded with
+ * dlopen at the first call; W_UK: this library's tcgen05 kernel); the
+ * RMSNorm is exact as stated.  A wait that gives up sets
+ * MLA_STATUS_WAIT_TIMEOUT in the device status word.
  *
  *   q_a, ld_qa  device bf16 rows, q_a values at columns 0..1535, row stride
  *               ld_qa elements (>= 1536, multiple of 8; the fused row:

@@ -98,6 +98,9 @@ namespace mla {
 void set_last_error(const char *msg) {
   snprintf(g_err, sizeof g_err, "%s", msg);
 }
+// Address of the device status word on the current device (for the entry
+// points of other translation units).
+int status_word(unsigned int **out) { return status_ptr(out); }
 }  // namespace mla
 
 extern "C" {

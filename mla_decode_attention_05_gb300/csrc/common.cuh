@@ -167,4 +167,5 @@ struct KvInsertParams {
 };
 cudaError_t launch_kv_insert(const KvInsertParams &p, cudaStream_t stream);
 void set_last_error(const char *msg);
+int status_word(unsigned int **out);
 }  // namespace mla

@@ -10,11 +10,13 @@
 //   S = sum x_i^2 (exact, rounded once to fp32), mean = fp32(fp32(S / 1536)
 //   + eps), r = fp32(1 / fp32(sqrt(mean))) (0 if mean == 0),
 //   xq_i = bf16(fp32(fp32(x_i * w_i) * r)).
-// The two contractions are plain bf16 GEMMs with fp32 accumulation (one
-// GEMM for Q_B, one strided-batched GEMM over heads for W_UK), run by cuBLAS,
-// which this file loads at the first call (dlopen) so that the rest of the
-// library does not depend on it; the RoPE rows are copied by a small kernel.
+// Q_B is a plain bf16 GEMM with fp32 accumulation, run by cuBLAS, which this
+// file loads at the first call (dlopen) so that the rest of the library does
+// not depend on it.  W_UK and the RoPE-row copy are one tcgen05 kernel of
+// this library (wuk_kernel below).
 #include <cublas_v2.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <dlfcn.h>
 
 #include <cstdio>
@@ -22,9 +24,12 @@
 
 #include "common.cuh"
 #include "exact_sum.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 namespace {
+
+using namespace ptx;
 
 constexpr int D_QA = 1536;
 constexpr int QB_ROWS = 192;
@@ -33,6 +38,8 @@ constexpr int kWarps = 8;
 constexpr int kChunks = D_QA / 8 / 32;  // 16-byte chunks per lane: 6
 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+std::mutex g_mu_enc;
 
 // One warp per token.  Lane l holds 16-byte chunks l, l + 32, ..., l + 160 of
 // the row, so every warp-wide load and store covers 512 contiguous bytes.
@@ -75,13 +82,144 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// q[n][h][512 + i] = qb[n][h * 192 + 128 + i], i < 64: one thread per 16 bytes.
-__global__ void rope_copy_kernel(const __nv_bfloat16 *qb, __nv_bfloat16 *q, int NH) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= NH * 8) return;
-  const int row = i >> 3, c = i & 7;
-  const uint4 v = *reinterpret_cast<const uint4 *>(qb + (size_t)row * QB_ROWS + D_NOPE + 8 * c);
-  *reinterpret_cast<uint4 *>(q + (size_t)row * D_QK + D_V + 8 * c) = v;
+// ---- W_UK and the RoPE rows: one CTA per (head, 256 latent columns, block
+// of 128 tokens) -----------------------------------------------------------
+//
+// q[n][h][l] = bf16(sum_{p<128} qb[n][h*192 + p] * W_UK[h][p][l]) as one
+// tcgen05 GEMM per CTA: M = 128 token rows (rows past N read as zeros), N =
+// 256 latent columns, K = 128.  A = the tokens' no-PE rows of qb, K-major;
+// B = the CTA's 256 columns of W_UK[h], read MN-major: both arrive as
+// 128-byte swizzled TMA boxes of 64 columns x 128 rows (16 KB).  D (128 x
+// 256 fp32) takes 256 TMEM columns and two CTAs share an SM, so a decode
+// batch (up to 128 tokens, 128 heads) runs in one wave: each CTA's chain of
+// load, MMA and store is paid once.  The CTAs of the first column half copy
+// the tokens' 64 RoPE values of qb after the latent columns while their
+// loads are in flight; four warps then read their 32 rows of D back, round
+// to bf16 and store them.
+constexpr int kWukThreads = 128;
+constexpr uint32_t kBoxBytes = 128 * 128;               // 64 bf16 columns x 128 rows
+constexpr uint32_t OFF_W = 0;                           // 4 boxes: latent columns col0 + 64j
+constexpr uint32_t OFF_A = 4 * kBoxBytes;               // 2 boxes: no-PE rows 0..63, 64..127
+constexpr uint32_t OFF_WBAR = OFF_A + 2 * kBoxBytes;    // full, done, tmem base
+constexpr uint32_t kWukSmem = OFF_WBAR + 64 + 1024;     // + slack for the 1024-byte alignment
+constexpr uint32_t IDESC_WUK = idesc_bf16_f32(128, 256, false, true);
+constexpr uint64_t kWukWaitNs = 2000000000ull;
+
+__global__ void __launch_bounds__(kWukThreads, 1)
+    wuk_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap a_map,
+               const __nv_bfloat16 *qb, __nv_bfloat16 *q, int N, int H, unsigned int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + OFF_WBAR);
+  uint64_t *done = full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, col0 = blockIdx.y * 256, n0 = blockIdx.z * 128;
+  int abort_flag = 0;  // the waits below give up only on their time limit
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(smem_u32(full), 1);
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init_cluster();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sw = smem_u32(base + OFF_W), sa = smem_u32(base + OFF_A);
+  const int n = n0 + warp * 32 + lane;
+  __nv_bfloat16 *qrow = q + ((size_t)n * H + h) * D_QK;
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(smem_u32(full), 6 * kBoxBytes);
+    for (int j = 0; j < 4; j++) tma_load_2d(sw + j * kBoxBytes, &w_map, smem_u32(full), col0 + 64 * j, 128 * h, pol);
+    for (int j = 0; j < 2; j++)
+      tma_load_2d(sa + j * kBoxBytes, &a_map, smem_u32(full), h * 192 + 64 * j, n0, policy_evict_normal());
+    if (mbar_wait<false>(smem_u32(full), 0, &abort_flag, kWukWaitNs)) {
+      tc_fence_after();
+      for (int k = 0; k < 8; k++) {
+        const uint64_t ad = smem_desc_sw128(sa + (k >> 2) * kBoxBytes + (k & 3) * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(sw + k * 16 * 128, kBoxBytes, 1024);
+        mma_ss(tmem, ad, bd, IDESC_WUK, k ? 1u : 0u);
+      }
+      mma_commit(smem_u32(done));
+    } else {
+      atomicOr(status, MLA_STATUS_WAIT_TIMEOUT);
+      mbar_arrive(smem_u32(done));  // nothing was issued: release the waiters
+    }
+  }
+  if (n < N && col0 == 0) {  // the RoPE rows, while the loads and MMAs run
+    const uint4 *src = reinterpret_cast<const uint4 *>(qb + (size_t)n * H * QB_ROWS + h * QB_ROWS + D_NOPE);
+    uint4 *dst = reinterpret_cast<uint4 *>(qrow + D_V);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) v[j] = src[j];
+#pragma unroll
+    for (int j = 0; j < 8; j++) dst[j] = v[j];
+  }
+  const bool ok = mbar_wait<false>(smem_u32(done), 0, &abort_flag, kWukWaitNs);
+  if (!ok && lane == 0) atomicOr(status, MLA_STATUS_WAIT_TIMEOUT);
+  tc_fence_after();
+  const bool live = ok && n < N;
+  for (int c = 0; c < 8; c++) {
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * c, v);  // warp-wide
+    tmem_wait_ld();
+    if (!live) continue;
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      w[j] = *reinterpret_cast<uint32_t *>(&b2);
+    }
+    uint4 *d4 = reinterpret_cast<uint4 *>(qrow + col0 + 32 * c);
+#pragma unroll
+    for (int j = 0; j < 4; j++) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+  if (!ok) {  // a wait gave up: let copies or MMAs still in flight land before the CTA exits
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lock(g_mu_enc);
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult qr;
+    void *f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// A 2-D bf16 tensor map [rows][cols] (row stride ld elements) with 64 x 128
+// boxes and 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // cuBLAS, loaded at first use (the C entry points, by name).
@@ -184,15 +322,16 @@ int mla_query_absorb(const void *q_a, int ld_qa, const void *w_qa, float eps, co
                D_QA, &zero, qb, CUDA_R_16BF, H * QB_ROWS, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) !=
       CUBLAS_STATUS_SUCCESS)
     return fail(MLA_ERR_CUDA, "cublasGemmEx (Q_B) failed");
-  // W_UK per head: q[n][h][l] = sum_p qb[n][h*192 + p] W_UK[h][p][l], p < 128;
-  // column-major per head: (512 x N, ld H*576) = W_UK[h] (512 x 128, ld 512)
-  // * qb_nope (128 x N, ld H*192)
-  if (cb->gemm_sb(hd, CUBLAS_OP_N, CUBLAS_OP_N, D_V, N, D_NOPE, &one, w_uk, CUDA_R_16BF, D_V,
-                  (long long)D_NOPE * D_V, qb, CUDA_R_16BF, H * QB_ROWS, QB_ROWS, &zero, qo, CUDA_R_16BF, H * D_QK,
-                  D_QK, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return fail(MLA_ERR_CUDA, "cublasGemmStridedBatchedEx (W_UK) failed");
-  const int nh = N * H;
-  rope_copy_kernel<<<(nh * 8 + 255) / 256, 256, 0, s>>>(qb, qo, nh);
+  // W_UK and the RoPE rows
+  CUtensorMap w_map, a_map;
+  if (!make_map(&w_map, w_uk, D_V, (uint64_t)H * D_NOPE, D_V) ||
+      !make_map(&a_map, qb, (uint64_t)H * QB_ROWS, (uint64_t)N, (uint64_t)H * QB_ROWS))
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  unsigned int *st = nullptr;
+  if (status_word(&st) != MLA_OK) return fail(MLA_ERR_CUDA, "device status word unavailable");
+  e = cudaFuncSetAttribute(wuk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWukSmem);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
+  wuk_kernel<<<dim3(H, D_V / 256, (N + 127) / 128), kWukThreads, kWukSmem, s>>>(w_map, a_map, qb, qo, N, H, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   set_last_error("");
