@@ -1059,9 +1059,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   cluster_sync();  // the peer's barriers exist before any remote arrive or copy
   const uint32_t tmem = br.tmem_base;
   // Everything above overlaps the kernel before this one (the schedule);
-  // no input is read before this point.
+  // no input is read before this point.  The combine kernel may launch once
+  // every CTA has finished its pieces (grid_dep_trigger below): launched
+  // earlier, its blocks would only sit beside these CTAs waiting.
   grid_dep_wait();
-  grid_dep_trigger();
 
   if (kGather) {
     if (warp == 0 || warp == 3) producer_gather(c, &q_map, warp == 0 ? lane : 32 + lane);
@@ -1085,6 +1086,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  grid_dep_trigger();
   if (br.abort) {  // a bounded wait gave up: let copies / MMAs in flight drain
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < 2000000ull) {
