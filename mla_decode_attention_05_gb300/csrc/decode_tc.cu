@@ -51,7 +51,7 @@ namespace {
 using namespace ptx;
 
 // 12 warps, plus a 13th in the gather kernel, where warps 0 and 3 gather
-__host__ __device__ constexpr int threads_of(bool gather) { return gather ? 416 : 384; }
+__host__ __device__ constexpr int threads_of(bool gather) { return gather ? 480 : 384; }
 __host__ __device__ constexpr int waiter_warp(bool gather) { return gather ? 12 : 3; }
 constexpr int kSoftmaxWarps = 8;
 constexpr int kBlkBytes = PAGE * 128;             // 64 tokens x 64 dims bf16, 128-byte swizzle
@@ -293,38 +293,55 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-constexpr int kGatherThreads = 64;
+// Row gather: two threads per key slot (128 threads in warps 0, 3, 13, 14).
+constexpr int kGatherThreads = 128;
 
-// Pool row of key slot pi of tile `tile` of an item (the top-k index or the
-// position, through the block table, with bounds checks), or -1; *n gets
-// the key index (or -1) for the gathered-index record.
-__device__ __forceinline__ long long gather_row(const DecodeParams &p, const Item &it, int t_item, int sk,
-                                                int tile, int pi, int *n_out) {
-  int n = -1;
-  if (p.topk_len > 0) {
-    const int slot = tile * PAGE + pi;
-    if (slot < p.topk_len) {
-      int id = __ldg(p.topk + ((size_t)it.b * p.T + t_item) * p.topk_len + slot);
-      if (id >= sk || id < -1) {
-        atomicOr(p.status, MLA_STATUS_BAD_TOPK);
-        id = -1;
-      }
-      n = id;
-    }
-  } else {
-    const int pos = tile * PAGE + pi;
-    if (pos < it.kv_len) n = pos;
+// Pool row of key slot pi of tile `tile` of an item: the top-k index or the
+// position, through the block table, with bounds checks; -1 for none.  It
+// takes two dependent loads (index, then block-table entry), so the gather
+// producer runs it as a pipeline over tiles: slot_id loads tile t+2's index,
+// slot_key checks tile t+1's and slot_page loads its block-table entry, and
+// slot_row resolves tile t from values loaded one and two tiles earlier.
+
+// Raw index of the slot (-2: past the item's keys).
+__device__ __forceinline__ int slot_id(const DecodeParams &p, const Item &it, int t_item, int tile, int pi) {
+  const int slot = tile * PAGE + pi;
+  if (p.topk_len > 0)
+    return slot < p.topk_len ? __ldg(p.topk + ((size_t)it.b * p.T + t_item) * p.topk_len + slot) : -2;
+  return slot < it.kv_len ? slot : -2;
+}
+
+// Key index within the sequence, or -1 (an out-of-range top-k index sets
+// MLA_STATUS_BAD_TOPK).
+__device__ __forceinline__ int slot_key(const DecodeParams &p, int id, int sk) {
+  if (id == -2) return -1;
+  if (p.topk_len > 0 && (id >= sk || id < -1)) {
+    atomicOr(p.status, MLA_STATUS_BAD_TOPK);
+    return -1;
   }
-  long long row = -1;
-  if (n >= 0) {
-    const int pg = page_of(p, it.b, n / PAGE);
-    if (pg < 0)
-      n = -1;
-    else
-      row = (long long)pg * PAGE + (n % PAGE);
+  return id;
+}
+
+// Block-table entry of key n (loaded, not yet checked), or -1.
+__device__ __forceinline__ int slot_page(const DecodeParams &p, int b, int n) {
+  if (n < 0) return -1;
+  if (n / PAGE >= p.max_pages) {
+    atomicOr(p.status, MLA_STATUS_BAD_SEQLEN);
+    return -1;
   }
-  *n_out = n;
-  return row;
+  return __ldg(p.block_table + (size_t)b * p.max_pages + n / PAGE);
+}
+
+// The pool row of key n in page pg; n becomes -1 when there is none (a page
+// outside the pool sets MLA_STATUS_BAD_PAGE).
+__device__ __forceinline__ long long slot_row(const DecodeParams &p, int &n, int pg) {
+  if (n < 0) return -1;
+  if (pg < 0 || pg >= p.num_pages) {
+    if (pg >= 0 || n / PAGE < p.max_pages) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+    n = -1;
+    return -1;
+  }
+  return (long long)pg * PAGE + (n % PAGE);
 }
 
 // 16-byte asynchronous copy global -> shared (cp.async); with ok false it
@@ -345,7 +362,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-constexpr uint32_t kGatherBar = 2;  // named barrier of the 64 gather threads
+constexpr uint32_t kGatherBar = 2;  // named barrier of the 128 gather threads
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
   asm volatile(
@@ -359,23 +376,43 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // rope), 128-byte swizzled (row pi of block kb at kb*8192 + pi*128, chunk j
 // at ((j ^ (pi & 7)) << 4)).
 //
-// FP8 rows: each thread brings its whole row (640 bytes on rank 0, the 512
-// e4m3 bytes on rank 1) with one bulk copy into a raw staging area at the
-// start of the stage (row pi at pi * rowbytes), completing on raw_bar;
-// thousands of 16-byte requests for random rows would leave the SM only a
-// few KB in flight.  Then each thread dequantises its row: the blocks that
-// lie past the staging area first, then, after all 64 threads have read
-// their staged bytes into registers, the blocks that overwrite it.
-// bf16 rows are copied 16 bytes at a time straight into place.
+// FP8 rows: the row's first thread brings the whole row (640 bytes on rank
+// 0, the 512 e4m3 bytes on rank 1) with one bulk copy into a raw staging
+// area at the start of the stage (row pi at pi * rowbytes), completing on
+// raw_bar (issue_raw_row, one tile ahead); thousands of 16-byte requests for
+// random rows would leave the SM only a few KB in flight.  Then the row's
+// two threads dequantise it, each
+// half of its column blocks: the blocks that lie past the staging area
+// first, then, after all gather threads have read their staged bytes into
+// registers, the blocks that overwrite it.  bf16 rows are copied 16 bytes at
+// a time straight into place, the blocks shared between the two threads.
+// FP8 rows: start the copy of the slot's raw row into the stage's staging
+// area (the row's first thread; the second only arrives), completing on
+// raw_bar.  Called a tile ahead of the dequantisation.
+__device__ __forceinline__ void issue_raw_row(const Ctx &c, long long row, uint32_t st, int pi, int half, bool rope,
+                                              uint64_t *raw_bar) {
+  const uint32_t rowbytes = rope ? FP8_ROW : 512;
+  const uint32_t raw = st + pi * rowbytes;
+  const uint32_t rb = smem_u32(raw_bar);
+  if (half == 0 && row >= 0) {
+    mbar_arrive_expect_tx(rb, rowbytes);
+    bulk_g2s(raw, c.p->kv + row * FP8_ROW, rowbytes, rb);
+  } else {
+    if (half == 0)
+      for (uint32_t j = 0; j < rowbytes; j += 16) st_shared_v4(raw + j, make_uint4(0, 0, 0, 0));
+    mbar_arrive(rb);
+  }
+}
+
 __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long long row, uint32_t st, int pi,
-                                                    bool rope, uint64_t *raw_bar, uint32_t raw_par) {
+                                                    int half, bool rope, uint64_t *raw_bar, uint32_t raw_par) {
   const DecodeParams &p = *c.p;
   const bool ok = row >= 0;
   const int sw = pi & 7;
   if (!fp8) {
     const uint8_t *src = p.kv + (ok ? row : 0) * (D_QK * 2);
     const int nb = rope ? 9 : 8;
-    for (int kb = 0; kb < nb; kb++)
+    for (int kb = half; kb < nb; kb += 2)
 #pragma unroll
       for (int j = 0; j < 8; j++) cp_async16(st + kb * kBlkBytes + pi * 128 + ((j ^ sw) << 4), src + kb * 128 + j * 16, ok);
     cp_async_wait_all();
@@ -383,20 +420,14 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   }
   const uint32_t rowbytes = rope ? FP8_ROW : 512;
   const uint32_t raw = st + pi * rowbytes;
-  const uint32_t rb = smem_u32(raw_bar);
-  if (ok) {
-    mbar_arrive_expect_tx(rb, rowbytes);
-    bulk_g2s(raw, p.kv + row * FP8_ROW, rowbytes, rb);
-  } else {
-    for (uint32_t j = 0; j < rowbytes; j += 16) st_shared_v4(raw + j, make_uint4(0, 0, 0, 0));
-    mbar_arrive(rb);
-  }
   const float4 sc = ok ? __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4)) : make_float4(0, 0, 0, 0);
   if (!wait_or_abort(c, raw_bar, raw_par)) return false;
-  // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them; rank 1:
-  // bytes 0..32767, blocks 4-7 lie past them
+  // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them (half 0:
+  // 5, 6; half 1: 7 and the RoPE block); rank 1: bytes 0..32767, blocks 4-7
+  // lie past them (half 0: 4, 5; half 1: 6, 7)
   const int split = rope ? 5 : 4;
-  for (int kb = split; kb < 8; kb++)
+  const int hi0 = split + 2 * half, hi1 = half ? 8 : split + 2;
+  for (int kb = hi0; kb < hi1; kb++)
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       uint4 lo, hi;
@@ -404,18 +435,22 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
-  if (rope)
+  if (rope && half == 1)
 #pragma unroll
     for (int j = 0; j < 8; j++) st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + 512 + j * 16));
-  uint4 v[20];  // e4m3 bytes of blocks 0 .. split-1 (at most 5 x 64 bytes)
+  // blocks below the staging area: half 0 takes blocks [0, lo_split), half
+  // 1 [lo_split, split) (rank 0: 0-2 | 3-4; rank 1: 0-1 | 2-3)
+  const int lo_split = rope ? 3 : 2;
+  const int lo0 = half ? lo_split : 0, lo1 = half ? split : lo_split;
+  uint4 v[12];  // e4m3 bytes of this thread's blocks below the staging area (at most 3 x 64 bytes)
 #pragma unroll
-  for (int u = 0; u < 20; u++)
-    if (u < split * 4) v[u] = ld_shared_v4(raw + u * 16);
+  for (int u = 0; u < 12; u++)
+    if (u < (lo1 - lo0) * 4) v[u] = ld_shared_v4(raw + lo0 * 64 + u * 16);
   named_bar_sync(kGatherBar, kGatherThreads);  // every staged byte below the blocks has been read
 #pragma unroll
-  for (int u = 0; u < 20; u++) {
-    if (u >= split * 4) break;
-    const int kb = u >> 2, ch = 2 * (u & 3);
+  for (int u = 0; u < 12; u++) {
+    if (u >= (lo1 - lo0) * 4) break;
+    const int kb = lo0 + (u >> 2), ch = 2 * (u & 3);
     uint4 lo, hi;
     dequant16(v[u], kb < 2 ? sc.x : (kb < 4 ? sc.y : sc.z), lo, hi);
     st_shared_v4(st + kb * kBlkBytes + pi * 128 + ((ch ^ sw) << 4), lo);
@@ -424,12 +459,13 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   return true;
 }
 
-// Thread pi (0..63) of the gather warps (0 and 3) owns key slot pi of every
-// tile: it resolves the row and writes it, dequantised to bf16, into row pi
-// of each column block of the stage (9 blocks on rank 0, 8 on rank 1).
-// rank 0 also publishes the tile's validity mask and the gathered-index
-// record.
-__device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) {
+// Threads gt and gt + 64 (gt < 64) of the gather warps (0, 3, 13, 14) own
+// key slot pi = gt of every tile: both resolve the row and each writes half
+// of it, dequantised to bf16, into row pi of the column blocks of the stage
+// (9 blocks on rank 0, 8 on rank 1).  On rank 0 the first thread of the slot
+// also publishes the tile's validity mask and the gathered-index record.
+__device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) {
+  const int pi = gt & 63, half = gt >> 6;
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format == MLA_KV_FP8_E4M3;
@@ -446,9 +482,9 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         const uint32_t s = sq % 3;
         bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1);
         if (ok) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1);
-        if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;  // all 64 give up together
+        if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;  // all gather threads give up together
         const uint32_t bar = smem_u32(&br.kv_full[s]);
-        if (pi == 0) {
+        if (gt == 0) {
           mbar_arrive_expect_tx(bar, kStage0Bytes);
           tma_load_3d(kv0 + s * kStage0Bytes, q_map, bar, 0, qrow + 64 * qh, 0, policy_evict_first());
         } else {
@@ -458,11 +494,45 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         mbar_arrive(smem_u32(&br.raw_full[s]));  // keeps the raw barrier's phase in step with the stage
       }
     }
+    // row pipeline (see slot_id): n0 / pg0 and n1 / pg1 = key and
+    // block-table entry of this tile and the next, id2 = raw index of the one
+    // after; each iteration loads the index three tiles ahead and the
+    // block-table entry two ahead
+    int n0 = t0 < t1 ? slot_key(p, slot_id(p, it, t_item, t0, pi), sk) : -1;
+    int pg0 = slot_page(p, it.b, n0);
+    int n1 = t0 + 1 < t1 ? slot_key(p, slot_id(p, it, t_item, t0 + 1, pi), sk) : -1;
+    int pg1 = slot_page(p, it.b, n1);
+    int id2 = t0 + 2 < t1 ? slot_id(p, it, t_item, t0 + 2, pi) : -2;
+    // FP8 rows: the raw copies of a tile are issued one tile ahead, into
+    // the tile's own stage once it is free
+    auto claim_stage = [&](uint32_t q) -> bool {  // stage of sequence number q is free (all threads agree)
+      const uint32_t ss = q % 3;
+      bool ok = wait_or_abort(c, &br.kv_empty[ss], ((q / 3) & 1) ^ 1);
+      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[ss], ((q / 3) & 1) ^ 1);
+      return !bar_red_or(kGatherBar, kGatherThreads, !ok);
+    };
+    long long row_cur = -1;
+    if (t0 < t1) {
+      int n = n0;
+      row_cur = slot_row(p, n, pg0);
+      if (fp8) {
+        if (!claim_stage(sq)) return false;
+        issue_raw_row(c, row_cur, kv0 + (sq % 3) * stage_bytes, pi, half, c.rank == 0, &br.raw_full[sq % 3]);
+      }
+    }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
       const uint32_t s = sq % 3;
-      int n;
-      const long long row = gather_row(p, it, t_item, sk, tile, pi, &n);
-      if (c.rank == 0) {
+      const int id3 = tile + 3 < t1 ? slot_id(p, it, t_item, tile + 3, pi) : -2;
+      const int n2 = slot_key(p, id2, sk);
+      const int pg2 = slot_page(p, it.b, n2);
+      int n = n0;
+      const long long row = slot_row(p, n, pg0);  // == row_cur
+      n0 = n1;
+      pg0 = pg1;
+      n1 = n2;
+      pg1 = pg2;
+      id2 = id3;
+      if (c.rank == 0 && half == 0) {
         const uint32_t bits = __ballot_sync(0xffffffffu, row >= 0);
         const uint32_t mi = g % kMaskRing;
         if ((pi & 31) == 0) br.mask[mi][pi >> 5] = bits;
@@ -473,16 +543,26 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int pi) 
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1);
-      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1);
-      // all 64 threads agree before the barriers inside the row copy
-      if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
-      ok = gather_row_to_stage(c, fp8, row, kv0 + s * stage_bytes, pi, c.rank == 0, &br.raw_full[s], (sq / 3) & 1);
+      if (fp8) {
+        // the next tile's raw rows start landing while this one is dequantised
+        if (tile + 1 < t1) {
+          int nn = n0;
+          const long long row_next = slot_row(p, nn, pg0);
+          if (!claim_stage(sq + 1)) return false;
+          issue_raw_row(c, row_next, kv0 + ((sq + 1) % 3) * stage_bytes, pi, half, c.rank == 0,
+                        &br.raw_full[(sq + 1) % 3]);
+        }
+      } else if (!claim_stage(sq)) {
+        return false;
+      }
+      bool ok = gather_row_to_stage(c, fp8, row, kv0 + s * stage_bytes, pi, half, c.rank == 0, &br.raw_full[s],
+                                    (sq / 3) & 1);
       if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
       if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
     }
+    (void)row_cur;
     return true;
   });
 }
@@ -1065,7 +1145,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   grid_dep_wait();
 
   if (kGather) {
-    if (warp == 0 || warp == 3) producer_gather(c, &q_map, warp == 0 ? lane : 32 + lane);
+    if (warp == 0 || warp == 3 || warp == 13 || warp == 14)
+      producer_gather(c, &q_map, (warp == 0 ? 0 : warp == 3 ? 32 : warp == 13 ? 64 : 96) + lane);
   } else if (warp == 0) {
     producer_tma(c, rank == 0 ? &k_map : &v_map, &kb_map, &q_map, lane);
   }
