@@ -404,8 +404,15 @@ __device__ __forceinline__ void issue_raw_row(const Ctx &c, long long row, uint3
   }
 }
 
+// The four per-128 scales of an FP8 row (zeros for no row), loaded a tile
+// ahead of their use.
+__device__ __forceinline__ float4 row_scales(const DecodeParams &p, long long row) {
+  return row >= 0 ? __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4)) : make_float4(0, 0, 0, 0);
+}
+
 __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long long row, uint32_t st, int pi,
-                                                    int half, bool rope, uint64_t *raw_bar, uint32_t raw_par) {
+                                                    int half, bool rope, uint64_t *raw_bar, uint32_t raw_par,
+                                                    float4 sc) {
   const DecodeParams &p = *c.p;
   const bool ok = row >= 0;
   const int sw = pi & 7;
@@ -420,7 +427,6 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   }
   const uint32_t rowbytes = rope ? FP8_ROW : 512;
   const uint32_t raw = st + pi * rowbytes;
-  const float4 sc = ok ? __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4)) : make_float4(0, 0, 0, 0);
   if (!wait_or_abort(c, raw_bar, raw_par)) return false;
   // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them (half 0:
   // 5, 6; half 1: 7 and the RoPE block); rank 1: bytes 0..32767, blocks 4-7
@@ -512,10 +518,12 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       return !bar_red_or(kGatherBar, kGatherThreads, !ok);
     };
     long long row_cur = -1;
+    float4 sc_cur = make_float4(0, 0, 0, 0);
     if (t0 < t1) {
       int n = n0;
       row_cur = slot_row(p, n, pg0);
       if (fp8) {
+        sc_cur = row_scales(p, row_cur);
         if (!claim_stage(sq)) return false;
         issue_raw_row(c, row_cur, kv0 + (sq % 3) * stage_bytes, pi, half, c.rank == 0, &br.raw_full[sq % 3]);
       }
@@ -543,11 +551,14 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
+      float4 sc_next = make_float4(0, 0, 0, 0);
       if (fp8) {
-        // the next tile's raw rows start landing while this one is dequantised
+        // the next tile's raw rows and scales start landing while this one
+        // is dequantised
         if (tile + 1 < t1) {
           int nn = n0;
           const long long row_next = slot_row(p, nn, pg0);
+          sc_next = row_scales(p, row_next);
           if (!claim_stage(sq + 1)) return false;
           issue_raw_row(c, row_next, kv0 + ((sq + 1) % 3) * stage_bytes, pi, half, c.rank == 0,
                         &br.raw_full[(sq + 1) % 3]);
@@ -556,7 +567,8 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         return false;
       }
       bool ok = gather_row_to_stage(c, fp8, row, kv0 + s * stage_bytes, pi, half, c.rank == 0, &br.raw_full[s],
-                                    (sq / 3) & 1);
+                                    (sq / 3) & 1, sc_cur);
+      sc_cur = sc_next;
       if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
