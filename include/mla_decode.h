@@ -152,8 +152,12 @@ size_t mla_decode_workspace_bytes(int B, int H, int T, int topk, int num_parts);
  *   out            device bf16 [B][T][H][512], written
  *   lse            device fp32 [B][H][T], written (natural log)
  *
- * Launches the decode kernel and, when some item was split over several
- * workers, the LSE combine kernel, both on `stream`.  Cache rows past s_k in
+ * Launches the decode kernel and the LSE combine kernel (which merges the
+ * items split over several workers) on `stream`, both as programmatic
+ * dependents of the kernel before them: the decode kernel sets itself up
+ * while the previous kernel of the stream (normally mla_decode_metadata's)
+ * finishes and reads no input before that kernel has completed; the
+ * combine kernel launches as the decode kernel's CTAs finish.  Cache rows past s_k in
  * a sequence's last page are read but carry zero weight; they must hold
  * finite values (a NaN there would reach `out` through 0 * NaN).
  */
@@ -312,7 +316,8 @@ int mla_device_status(uint32_t *status);
 /*
  * Profiling hook: when both are non-NULL cudaEvent_t handles, every later
  * mla_decode call on this thread records `before` on its stream right before
- * the decode kernel launch and `after` right after it (the combine kernel
+ * the decode kernel launch and `after` right after it (an event between
+ * kernels keeps the next one from starting early; the combine kernel
  * is outside).  Pass NULL, NULL to stop.  Returns MLA_OK.
  */
 int mla_profile_events(void *before, void *after);

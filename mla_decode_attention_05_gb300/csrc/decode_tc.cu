@@ -17,20 +17,20 @@
 //
 // Only P crosses between the SMs, never a partial S.  P travels through L2:
 // the softmax threads of rank 0 write P and the per-row rescale factors into
-// a small per-worker ring in the workspace, and rank 1 bulk-copies each slot
-// into shared memory.  P is stored chunk-major, [8 chunks of 8 tokens][128
+// a small per-worker ring in the workspace, and rank 1's epilogue warps copy
+// each slot into shared memory with plain L2 loads.  P is stored chunk-major, [8 chunks of 8 tokens][128
 // rows][16 bytes], so each warp store covers 512 contiguous bytes, and that
 // same image is the A operand of rank 1's MMA (K-major, no swizzle: core
 // matrices of 8 rows x 16 bytes, 2048 bytes apart along K, 128 along M).  The direct SM-to-SM
 // path (DSMEM) is several times narrower than that per SM.
 //
-// Per CTA, 384 threads (416 in the gather kernel):
+// Per CTA, 384 threads (480 in the gather kernel):
 //   warp 0      producer: one 4-D TMA per page (rank 0: the 9 column blocks
-//               into a 3-stage ring; rank 1: the 8 V blocks), or with warp 3
-//               the row gather / FP8 dequantisation into the same layout
+//               into a 3-stage ring; rank 1: the 8 V blocks), or with warps
+//               3, 13 and 14 the row gather / FP8 dequantisation into the
+//               same layout
 //   warp 1      TMEM allocation and the MMA warp (one elected lane issues)
-//   warp 2      rank 0: publishes written P slots to rank 1;
-//               rank 1: P loader (ring slot -> shared memory)
+//   warp 2      rank 0: publishes written P slots to rank 1; rank 1: idle
 //   warp 3      the MMA warp's waiter (warp 12 in the gather kernel)
 //   warps 4-11  rank 0: softmax, two threads per query row (TMEM lane):
 //               warps 4-7 take tokens 0-31 of each tile, warps 8-11 32-63
@@ -50,7 +50,8 @@ namespace {
 
 using namespace ptx;
 
-// 12 warps, plus a 13th in the gather kernel, where warps 0 and 3 gather
+// 12 warps, 15 in the gather kernel, where warps 0, 3, 13 and 14 gather and
+// warp 12 waits for the MMA warp
 __host__ __device__ constexpr int threads_of(bool gather) { return gather ? 480 : 384; }
 __host__ __device__ constexpr int waiter_warp(bool gather) { return gather ? 12 : 3; }
 constexpr int kSoftmaxWarps = 8;
@@ -265,7 +266,7 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
   });
 }
 
-// ---- producer: row gather / FP8 dequantisation (warps 0 and 3) --------------------
+// ---- producer: row gather / FP8 dequantisation (warps 0, 3, 13, 14) -------------------
 
 __device__ __forceinline__ void dequant16(uint4 v, float sc, uint4 &lo, uint4 &hi) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -534,7 +535,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       const int n2 = slot_key(p, id2, sk);
       const int pg2 = slot_page(p, it.b, n2);
       int n = n0;
-      const long long row = slot_row(p, n, pg0);  // == row_cur
+      const long long row = slot_row(p, n, pg0);
       n0 = n1;
       pg0 = pg1;
       n1 = n2;
@@ -574,7 +575,6 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       mbar_arrive(smem_u32(&br.kv_full[s]));
       if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
     }
-    (void)row_cur;
     return true;
   });
 }
