@@ -151,6 +151,15 @@ def test_more_workers_than_fit_at_once(mla, oracle_mod):
     G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
 
 
+def test_largest_rows_per_sequence_causal(mla, oracle_mod):
+    """T = 16 query tokens x H = 128 heads = 2048 rows per sequence (16
+    items each), causal, ragged lengths: every row against the oracle."""
+    w = make_workload("t16h128", 2, 16, 128, [200, 77], seed=31, causal=True)
+    res = G.run(w)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
+    _status_clean(mla)
+
+
 def test_metadata_bit_exact(mla):
     """Device schedule == the plain-Python statement of the rule."""
     from oracle import schedule as S

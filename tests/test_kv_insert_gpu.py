@@ -149,3 +149,26 @@ def test_decode_reads_what_insert_wrote():
     got_l = np.array([lse[b, h, t].item() for b, t, h in rows])
     assert np.abs(got_o - ref_o).max() <= TOL_O
     assert np.abs(got_l - ref_l).max() <= TOL_LSE
+
+
+def test_bench_size_insert_sampled():
+    """The bench's insert (262144 tokens filling a 4096-page FP8 cache):
+    3000 sampled tokens' rows and scales bit-exact against the oracle."""
+    import mla_decode_attention_05_gb300 as mla
+    inp = W.make_insert_inputs(262144, 4096, seed=4242, skip_every=0)
+    kv_c, k_pe, w, sl = _dev_inputs(inp)
+    cache = torch.zeros((4096, 64, 640), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((4096, 64, 4), dtype=torch.float32, device="cuda")
+    mla.device_status()
+    mla.kv_insert(kv_c, k_pe, w, sl, cache, eps=inp.eps, kv_scales=sc)
+    torch.cuda.synchronize()
+    assert mla.device_status() == 0
+    rng = np.random.default_rng(1)
+    pick = rng.choice(inp.N, 3000, replace=False)
+    got_c = cache.view(-1, 640)[torch.from_numpy(inp.slots[pick]).cuda()].cpu().numpy()
+    got_s = sc.view(-1, 4)[torch.from_numpy(inp.slots[pick]).cuda()].cpu().numpy()
+    for k, j in enumerate(pick):
+        row, scl = K.insert_row(K.FMT_FP8_TILE, inp.qkv[j, W.KV_C_COL:W.KV_C_COL + 512],
+                                inp.qkv[j, W.K_PE_COL:W.K_PE_COL + 64], inp.w_kva, inp.eps)
+        np.testing.assert_array_equal(got_c[k], row)
+        np.testing.assert_array_equal(got_s[k].view(np.uint32), scl.view(np.uint32))
