@@ -53,6 +53,8 @@ extern "C" {
 #define MLA_KV_BF16 0     /* row = 576 bf16 (1152 bytes)                        */
 #define MLA_KV_FP8_E4M3 1 /* row = 512 e4m3 bytes + 64 bf16 RoPE (640 bytes),
                              plus 4 fp32 scales per row in kv_scales            */
+#define MLA_KV_FP8_E4M3_TENSOR 2 /* row = 576 e4m3 bytes, RoPE included (576 bytes),
+                                  one fp32 scale for the whole cache */
 
 /* Device status bits (mla_device_status). */
 #define MLA_STATUS_BAD_PAGE 1u      /* block_table entry outside [0, num_pages) */
@@ -132,8 +134,10 @@ size_t mla_decode_workspace_bytes(int B, int H, int T, int topk, int num_parts);
  *
  *   q              device bf16 [B][T][H][576]   (row-major, 16-byte aligned)
  *   kv_cache       device, MLA_KV_BF16: bf16 [num_pages][64][576];
- *                  MLA_KV_FP8_E4M3: bytes [num_pages][64][640] (16-byte aligned)
- *   kv_format      MLA_KV_BF16 or MLA_KV_FP8_E4M3
+ *                  MLA_KV_FP8_E4M3: bytes [num_pages][64][640];
+ *                  MLA_KV_FP8_E4M3_TENSOR: bytes [num_pages][64][576]
+ *                  (16-byte aligned)
+ *   kv_format      MLA_KV_BF16, MLA_KV_FP8_E4M3 or MLA_KV_FP8_E4M3_TENSOR
  *   num_pages      pages in the pool; page_size must be 64
  *   block_table    device int32 [B][max_pages]: page of the j-th 64 tokens
  *   cache_seqlens  device int32 [B]: s_k per sequence
@@ -143,8 +147,11 @@ size_t mla_decode_workspace_bytes(int B, int H, int T, int topk, int num_parts);
  *                  the kernel writes, per slot, the token position whose row
  *                  it loaded, or -1 for a slot it skipped
  *   kv_scales      device fp32 [num_pages][64][4] for MLA_KV_FP8_E4M3
- *                  (value = e4m3(byte) * kv_scales[page][slot][d / 128]),
- *                  else NULL
+ *                  (value = e4m3(byte) * kv_scales[page][slot][d / 128]);
+ *                  one device fp32 for MLA_KV_FP8_E4M3_TENSOR (value =
+ *                  e4m3(byte) * kv_scales[0] for all 576 values: the
+ *                  reciprocal of the k_scale_inv mla_kv_insert used); else
+ *                  NULL
  *   softmax_scale  > 0 (1/sqrt(192) for the 128 no-PE + 64 RoPE query dims)
  *   causal         0/1
  *   tile_md, num_splits, num_parts   from mla_decode_metadata
@@ -261,7 +268,6 @@ int mla_decode_noalloc(const void *q, const void *kv_cache, int kv_format,
  * outside [0, num_pages * page_size) other than -1 is skipped and sets
  * MLA_STATUS_BAD_PAGE.  Returns MLA_OK or a negative MLA_ERR_* code.
  */
-#define MLA_KV_FP8_E4M3_TENSOR 2
 int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, const void *w_kva, float eps,
                   const int64_t *slots, int N, void *kv_cache, int kv_format, int num_pages, int page_size,
                   float *kv_scales, const float *k_scale_inv, mla_stream_t stream);

@@ -156,8 +156,10 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
            gathered: Optional[torch.Tensor] = None):
     """MLA decode on the current stream -> (out bf16 [B,T,H,512], lse fp32 [B,H,T]).
 
-    q bf16 [B,T,H,576]; kv_cache bf16 [P,64,576] (bf16 rows) or uint8
-    [P,64,640] (e4m3 latent + bf16 RoPE rows, with kv_scales fp32 [P,64,4]);
+    q bf16 [B,T,H,576]; kv_cache bf16 [P,64,576] (bf16 rows), uint8
+    [P,64,640] (e4m3 latent + bf16 RoPE rows, with kv_scales fp32 [P,64,4]) or
+    uint8 [P,64,576] (all e4m3, with one fp32 scale in kv_scales: the value is
+    e4m3 x scale, i.e. the scale is 1 / the k_scale_inv kv_insert used);
     block_table int32 [B,max_pages]; cache_seqlens int32 [B]; topk_indices
     int32 [B,T,topk] or None.  tile_md/num_splits come from metadata() with
     the same arguments (computed here when omitted)."""
@@ -171,10 +173,16 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
         if kv_cache.dim() != 3 or kv_cache.shape[2] != D_QK:
             raise ValueError("bf16 kv_cache must be [P, 64, 576]")
     elif kv_cache.dtype == torch.uint8:
-        fmt = KV_FP8_E4M3
-        if kv_cache.dim() != 3 or kv_cache.shape[2] != FP8_ROW_BYTES:
-            raise ValueError("fp8 kv_cache must be uint8 [P, 64, 640]")
-        _need(kv_scales, "kv_scales", torch.float32, dev, 3)
+        if kv_cache.dim() != 3 or kv_cache.shape[2] not in (FP8_ROW_BYTES, D_QK):
+            raise ValueError("fp8 kv_cache must be uint8 [P, 64, 640] (per-128 scales) or [P, 64, 576] (per-tensor)")
+        if kv_cache.shape[2] == FP8_ROW_BYTES:
+            fmt = KV_FP8_E4M3
+            _need(kv_scales, "kv_scales", torch.float32, dev, 3)
+        else:
+            fmt = KV_FP8_E4M3_TENSOR
+            _need(kv_scales, "kv_scales", torch.float32, dev)
+            if kv_scales.numel() != 1:
+                raise ValueError("a per-tensor fp8 cache takes kv_scales with one fp32 scale")
     else:
         raise TypeError("kv_cache must be bfloat16 or uint8 (fp8 rows)")
     _need(kv_cache, "kv_cache", kv_cache.dtype, dev)
@@ -224,7 +232,10 @@ def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.T
     _need(q, "q", torch.bfloat16, ndim=4)
     dev = q.device
     B, T, H, _ = q.shape
-    fmt = KV_BF16 if kv_cache.dtype == torch.bfloat16 else KV_FP8_E4M3
+    if kv_cache.dtype == torch.bfloat16:
+        fmt = KV_BF16
+    else:
+        fmt = KV_FP8_E4M3 if kv_cache.shape[2] == FP8_ROW_BYTES else KV_FP8_E4M3_TENSOR
     topk = 0 if topk_indices is None else topk_indices.shape[2]
     if out is None:
         out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)

@@ -174,10 +174,12 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   if (!aligned(block_table, 4) || !aligned(cache_seqlens, 4) || !aligned(lse, 4) ||
       !aligned(tile_md, 4) || !aligned(num_splits, 4))
     return fail(MLA_ERR_INVALID_ARG, "int32/fp32 arrays must be 4-byte aligned");
-  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_E4M3)
+  if (kv_format != MLA_KV_BF16 && kv_format != MLA_KV_FP8_E4M3 && kv_format != MLA_KV_FP8_E4M3_TENSOR)
     return fail(MLA_ERR_INVALID_ARG, "kv_format = %d", kv_format);
   if (kv_format == MLA_KV_FP8_E4M3 && (!kv_scales || !aligned(kv_scales, 16)))
     return fail(MLA_ERR_INVALID_ARG, "FP8 cache needs 16-byte aligned kv_scales");
+  if (kv_format == MLA_KV_FP8_E4M3_TENSOR && (!kv_scales || !aligned(kv_scales, 4)))
+    return fail(MLA_ERR_INVALID_ARG, "per-tensor FP8 cache needs kv_scales (one fp32 scale)");
   if (page_size != MLA_PAGE_SIZE) return fail(MLA_ERR_UNSUPPORTED, "page_size = %d (only 64)", page_size);
   if (num_pages < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages/max_pages < 1");
   if ((topk > 0) != (topk_indices != nullptr))

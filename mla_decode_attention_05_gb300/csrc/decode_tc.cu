@@ -390,14 +390,21 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // FP8 rows: start the copy of the slot's raw row into the stage's staging
 // area (the row's first thread; the second only arrives), completing on
 // raw_bar.  Called a tile ahead of the dequantisation.
+// Bytes of an FP8 cache row: 640 (e4m3 latent + bf16 RoPE), or 576 in the
+// per-tensor format (all e4m3).
+__device__ __forceinline__ uint32_t fp8_row_bytes(const DecodeParams &p) {
+  return p.kv_format == MLA_KV_FP8_E4M3_TENSOR ? D_QK : FP8_ROW;
+}
+
 __device__ __forceinline__ void issue_raw_row(const Ctx &c, long long row, uint32_t st, int pi, int half, bool rope,
                                               uint64_t *raw_bar) {
-  const uint32_t rowbytes = rope ? FP8_ROW : 512;
+  const uint32_t stride = fp8_row_bytes(*c.p);
+  const uint32_t rowbytes = rope ? stride : 512;
   const uint32_t raw = st + pi * rowbytes;
   const uint32_t rb = smem_u32(raw_bar);
   if (half == 0 && row >= 0) {
     mbar_arrive_expect_tx(rb, rowbytes);
-    bulk_g2s(raw, c.p->kv + row * FP8_ROW, rowbytes, rb);
+    bulk_g2s(raw, c.p->kv + row * stride, rowbytes, rb);
   } else {
     if (half == 0)
       for (uint32_t j = 0; j < rowbytes; j += 16) st_shared_v4(raw + j, make_uint4(0, 0, 0, 0));
@@ -405,10 +412,15 @@ __device__ __forceinline__ void issue_raw_row(const Ctx &c, long long row, uint3
   }
 }
 
-// The four per-128 scales of an FP8 row (zeros for no row), loaded a tile
-// ahead of their use.
+// The four per-128 scales of an FP8 row (the one scale of a per-tensor
+// cache four times; zeros for no row), loaded a tile ahead of their use.
 __device__ __forceinline__ float4 row_scales(const DecodeParams &p, long long row) {
-  return row >= 0 ? __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4)) : make_float4(0, 0, 0, 0);
+  if (row < 0) return make_float4(0, 0, 0, 0);
+  if (p.kv_format == MLA_KV_FP8_E4M3_TENSOR) {
+    const float k = __ldg(p.kv_scales);
+    return make_float4(k, k, k, k);
+  }
+  return __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4));
 }
 
 __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long long row, uint32_t st, int pi,
@@ -426,7 +438,7 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
     cp_async_wait_all();
     return true;
   }
-  const uint32_t rowbytes = rope ? FP8_ROW : 512;
+  const uint32_t rowbytes = rope ? fp8_row_bytes(p) : 512;
   const uint32_t raw = st + pi * rowbytes;
   if (!wait_or_abort(c, raw_bar, raw_par)) return false;
   // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them (half 0:
@@ -442,9 +454,20 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
-  if (rope && half == 1)
+  if (rope && half == 1) {
+    if (p.kv_format == MLA_KV_FP8_E4M3_TENSOR) {  // 64 e4m3 RoPE values x the scale
 #pragma unroll
-    for (int j = 0; j < 8; j++) st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + 512 + j * 16));
+      for (int u = 0; u < 4; u++) {
+        uint4 lo, hi;
+        dequant16(ld_shared_v4(raw + 512 + u * 16), sc.x, lo, hi);
+        st_shared_v4(st + 8 * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
+        st_shared_v4(st + 8 * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
+      }
+    } else {  // 64 bf16 RoPE values, copied
+#pragma unroll
+      for (int j = 0; j < 8; j++) st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + 512 + j * 16));
+    }
+  }
   // blocks below the staging area: half 0 takes blocks [0, lo_split), half
   // 1 [lo_split, split) (rank 0: 0-2 | 3-4; rank 1: 0-1 | 2-3)
   const int lo_split = rope ? 3 : 2;
@@ -475,7 +498,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
   const int pi = gt & 63, half = gt >> 6;
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  const bool fp8 = p.kv_format == MLA_KV_FP8_E4M3;
+  const bool fp8 = p.kv_format != MLA_KV_BF16;
   const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   uint32_t g = 0, sq = 0;  // tiles; stages of the ring (rank 0: query stages too)

@@ -30,7 +30,9 @@
  * bits, subnormals at exponent 0, no infinities, and S.1111.111 = NaN.
  * FP8 rows: 512 e4m3 bytes then 64 bf16 RoPE values (640 bytes), with one
  * fp32 scale per 128-wide tile of the 512; the dequantised value is the exact
- * product e4m3(byte) * scale.
+ * product e4m3(byte) * scale.  Per-tensor FP8 rows (the layout vLLM's
+ * MlaQuery.insert writes): 576 e4m3 bytes, RoPE included, all dequantised
+ * with one fp32 scale (the reciprocal of the writer's k_scale_inv).
  *
  * Everything is plain double arithmetic; the only library calls are exp, log
  * and ldexp.  Row-level OpenMP parallelism does not change any result.
@@ -43,6 +45,7 @@
 #define ORACLE_D_QK 576
 #define ORACLE_D_V 512
 #define ORACLE_FP8_ROW 640
+#define ORACLE_FP8T_ROW 576
 
 double oracle_bf16_to_f64(uint16_t bits)
 {
@@ -69,11 +72,11 @@ double oracle_e4m3_to_f64(uint8_t code)
 
 /* The KV cache as the oracle sees it. */
 typedef struct {
-    const void *kv;           /* bf16 bits [P][page][576] or bytes [P][page][640] */
-    int kv_format;            /* 0 = bf16, 1 = fp8 e4m3 + bf16 rope */
+    const void *kv;           /* bf16 bits [P][page][576], bytes [P][page][640] or [P][page][576] */
+    int kv_format;            /* 0 = bf16, 1 = fp8 e4m3 + bf16 rope, 2 = per-tensor fp8 (576 e4m3) */
     int num_pages;
     int page_size;
-    const float *kv_scales;   /* fp8 only: [P][page][4] */
+    const float *kv_scales;   /* format 1: [P][page][4]; format 2: one scale */
     const int32_t *block_table;
     int max_pages;
 } oracle_cache;
@@ -91,6 +94,10 @@ static int load_key_row(const oracle_cache *c, int b, int n, double *row)
         const uint16_t *p = (const uint16_t *)c->kv + r * ORACLE_D_QK;
         for (int d = 0; d < ORACLE_D_QK; d++)
             row[d] = oracle_bf16_to_f64(p[d]);
+    } else if (c->kv_format == 2) {
+        const uint8_t *p = (const uint8_t *)c->kv + r * ORACLE_FP8T_ROW;
+        for (int d = 0; d < ORACLE_D_QK; d++)
+            row[d] = oracle_e4m3_to_f64(p[d]) * (double)c->kv_scales[0];
     } else {
         const uint8_t *p = (const uint8_t *)c->kv + r * ORACLE_FP8_ROW;
         const float *sc = c->kv_scales + r * 4;

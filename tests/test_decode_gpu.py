@@ -76,6 +76,8 @@ SMALL = [
     dict(B=3, T=1, H=128, seqlens=[0, 70, 0]),
     dict(B=2, T=1, H=64, seqlens=[500, 90], fp8=True),
     dict(B=2, T=2, H=64, seqlens=[300, 200], topk=100, topk_pad_count=9, fp8=True),
+    dict(B=2, T=1, H=64, seqlens=[500, 90], fp8_tensor=True),
+    dict(B=2, T=2, H=128, seqlens=[300, 200], topk=100, topk_pad_count=9, fp8_tensor=True),
     dict(B=2, T=1, H=128, seqlens=[400, 70], topk=64),
     dict(B=1, T=1, H=64, seqlens=[64], topk=1),
     dict(B=2, T=1, H=1, seqlens=[300, 65]),

@@ -172,3 +172,43 @@ def test_bench_size_insert_sampled():
                                 inp.qkv[j, W.K_PE_COL:W.K_PE_COL + 64], inp.w_kva, inp.eps)
         np.testing.assert_array_equal(got_c[k], row)
         np.testing.assert_array_equal(got_s[k].view(np.uint32), scl.view(np.uint32))
+
+
+def test_decode_reads_per_tensor_fp8_insert():
+    """The page's own cache layout end to end: insert every token of two
+    sequences as per-tensor FP8 rows (e4m3(v * k_scale_inv), RoPE included),
+    decode with the scale 1 / k_scale_inv: bytes equal the oracle's and the
+    attention matches the oracle's over the oracle-inserted cache."""
+    import mla_decode_attention_05_gb300 as mla
+    from oracle import decode_rows
+    from _gpu import TOL_LSE, TOL_O
+
+    w = W.make_workload("tensor_insert_decode", 2, 1, 64, [300, 129], seed=81, num_pages=12, fp8_tensor=True)
+    slots = np.concatenate([w.block_table[b, np.arange(n) // 64].astype(np.int64) * 64 + np.arange(n) % 64
+                            for b, n in enumerate(w.cache_seqlens)])
+    inp = W.make_insert_inputs(len(slots), w.num_pages, seed=82, skip_every=0, k_scale_inv=4.0)
+    inp.slots = slots
+    cache = w.kv.copy()
+    K.kv_insert(K.FMT_FP8_TENSOR, inp.qkv[:, W.KV_C_COL:], inp.qkv[:, W.K_PE_COL:], inp.w_kva, inp.eps,
+                slots, cache, None, inp.k_scale_inv)
+    w.kv = cache
+    w.kv_scales = np.array([np.float32(1.0) / np.float32(inp.k_scale_inv)], dtype=np.float32)
+
+    kv_c, k_pe, wk, sl = _dev_inputs(inp)
+    d_cache = torch.from_numpy(np.full_like(cache, SENTINEL)).cuda()
+    ksi = torch.tensor([inp.k_scale_inv], dtype=torch.float32, device="cuda")
+    mla.kv_insert(kv_c, k_pe, wk, sl, d_cache, eps=inp.eps, k_scale_inv=ksi, fp8_per_tensor=True)
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).cuda()
+    out, lse = mla.decode(q, d_cache, torch.from_numpy(w.block_table).cuda(),
+                          torch.from_numpy(w.cache_seqlens).cuda(), softmax_scale=w.softmax_scale,
+                          kv_scales=torch.from_numpy(w.kv_scales).cuda())
+    torch.cuda.synchronize()
+    live = np.zeros(cache.shape[:2], bool)
+    live.reshape(-1)[slots] = True
+    np.testing.assert_array_equal(d_cache.cpu().numpy()[live], cache[live])
+    rows = [(b, 0, h) for b in range(2) for h in (0, 17, 63)]
+    ref_o, ref_l = decode_rows(w, rows)
+    got_o = np.stack([out[b, t, h].float().cpu().numpy() for b, t, h in rows])
+    got_l = np.array([lse[b, h, t].item() for b, t, h in rows])
+    assert np.abs(got_o - ref_o).max() <= TOL_O
+    assert np.abs(got_l - ref_l).max() <= TOL_LSE

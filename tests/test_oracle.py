@@ -194,6 +194,41 @@ def test_fp8_dequant_is_product_with_scale(oracle_mod):
     np.testing.assert_allclose(lse[0, :, 0], rl, atol=1e-12, rtol=0)
 
 
+def test_per_tensor_fp8_rows_equal_bf16_rows_with_pow2_scale(oracle_mod):
+    """Per-tensor FP8 rows (576 e4m3 bytes, RoPE included, one scale): with a
+    power-of-two scale every dequantised value is exact in bf16, so the cache
+    and its bf16 image give identical results (catches a wrong row stride,
+    a RoPE part read as bf16, or a missing scale)."""
+    w8 = make_workload("tt", 2, 1, 4, [130, 64], seed=19, fp8_tensor=True)
+    w8.kv_scales = np.array([0.25], dtype=np.float32)
+    vals = torch.from_numpy(np.ascontiguousarray(w8.kv)).view(torch.float8_e4m3fn).double() * 0.25
+    kv = vals.to(torch.bfloat16)
+    assert torch.equal(kv.double(), vals)  # exact in bf16
+    wb = workloads.Workload(
+        name="as_bf16", B=w8.B, T=w8.T, H=w8.H, q=w8.q,
+        kv=kv.view(torch.int16).numpy().view(np.uint16), kv_format=workloads.KV_BF16,
+        kv_scales=None, block_table=w8.block_table, cache_seqlens=w8.cache_seqlens,
+        topk=w8.topk, softmax_scale=w8.softmax_scale, causal=w8.causal, seed=w8.seed)
+    o8, l8 = oracle_mod.decode_all(w8)
+    ob, lb = oracle_mod.decode_all(wb)
+    np.testing.assert_allclose(o8, ob, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(l8, lb, atol=1e-14, rtol=0)
+
+
+def test_per_tensor_fp8_dequant_is_product_with_scale(oracle_mod):
+    """Arbitrary scale: library attention on K = torch's e4m3 decode x the
+    scale in float64, all 576 values."""
+    w8 = make_workload("tt", 1, 1, 3, [100], seed=14, fp8_tensor=True)
+    out, lse = oracle_mod.decode_all(w8)
+    n = 100
+    pages = w8.block_table[0, np.arange(n) // 64]
+    rows = w8.kv[pages, np.arange(n) % 64]
+    K = torch.from_numpy(np.ascontiguousarray(rows)).view(torch.float8_e4m3fn).double() * float(w8.kv_scales[0])
+    ro, rl = _sdpa(_bf16_bits_to_f64(w8.q[0, 0]), K, w8.softmax_scale)
+    np.testing.assert_allclose(out[0, 0], ro, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[0, :, 0], rl, atol=1e-12, rtol=0)
+
+
 # --- invariants and closed forms ------------------------------------------------------
 
 def _set_rows(w, b, n_keys, rows_bits):

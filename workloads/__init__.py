@@ -22,6 +22,8 @@ Formats (all little-endian, raw bits):
   kv_scales    float32           [num_pages, 64, 4]: one scale per 128-wide
                tile of the no-RoPE latent; the dequantised value is
                e4m3(byte) * scale
+  kv (per-tensor fp8)  uint8     [num_pages, 64, 576]: all 576 values e4m3,
+               with kv_scales float32 [1], value = e4m3(byte) * scale
   block_table  int32             [B, max_pages]
   cache_seqlens int32            [B]
   topk         int32             [B, T, topk] token positions within the
@@ -43,6 +45,7 @@ PAGE = 64
 FP8_ROW_BYTES = 640
 KV_BF16 = 0
 KV_FP8 = 1
+KV_FP8_TENSOR = 2     # 576 e4m3 bytes per row (RoPE included), one scale for the whole cache
 
 
 @dataclasses.dataclass
@@ -184,6 +187,7 @@ def make_workload(
     topk_pad_frac: float = 0.0,
     topk_pad_count: Optional[int] = None,
     fp8: bool = False,
+    fp8_tensor: bool = False,
     causal: bool = False,
     softmax_scale: float = 1.0 / math.sqrt(192.0),
     seqlen_range: tuple = (1024, 32768),
@@ -238,7 +242,15 @@ def make_workload(
                     idx[pos] = -1
                 topk_arr[b, t] = idx
 
-    if not fp8:
+    if fp8_tensor:
+        # per-tensor FP8 rows (the layout of vLLM's MlaQuery.insert): every
+        # value, RoPE included, is e4m3(x / scale) for one scale
+        fmt = KV_FP8_TENSOR
+        scale = np.float32(g.uniform(0.5, 2.0, 1)[0])
+        x = g.normal_f32(num_pages * PAGE * D_QK, value_std).reshape(num_pages, PAGE, D_QK)
+        kv = _to_e4m3_bits(x / scale).reshape(num_pages, PAGE, D_QK)
+        scales = np.array([scale], dtype=np.float32)
+    elif not fp8:
         kv = _bf16_normal(g, (num_pages, PAGE, D_QK), value_std)
         fmt = KV_BF16
     else:
@@ -419,6 +431,8 @@ def make_query_inputs(N: int, H: int, *, seed: int, eps: float = 1e-6) -> QueryI
 def kv_bytes_per_token(kv_format: int) -> int:
     """Algorithmic bytes of one valid key: 576 bf16, or 512 e4m3 + 4 fp32
     scales + 64 bf16 RoPE."""
+    if kv_format == KV_FP8_TENSOR:
+        return D_QK
     return 2 * D_QK if kv_format == KV_BF16 else D_V + 16 + 2 * D_ROPE
 
 
