@@ -46,7 +46,7 @@ extern "C" {
 
 #define MLA_OK 0
 #define MLA_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or flag */
-#define MLA_ERR_UNSUPPORTED (-2) /* valid request this build does not serve   */
+#define MLA_ERR_UNSUPPORTED (-2) /* valid request this library does not serve */
 #define MLA_ERR_WORKSPACE (-3)   /* workspace null or smaller than required   */
 #define MLA_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed         */
 
@@ -62,7 +62,7 @@ extern "C" {
 #define MLA_STATUS_BAD_SEQLEN 4u    /* negative s_k, or more pages than max_pages */
 #define MLA_STATUS_WAIT_TIMEOUT 8u  /* a bounded device wait gave up            */
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define MLA_PAGE_SIZE 64
 #define MLA_MAX_HEADS 128
 #define MLA_MAX_QUERY_TOKENS 16
