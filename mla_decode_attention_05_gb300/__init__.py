@@ -111,8 +111,8 @@ def _need(t, name, dtype, device=None, ndim=None):
 
 
 def default_num_parts(device=None) -> int:
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
-    return _check(lib().mla_default_num_parts(dev.index))
+    idx = None if device is None else torch.device(device).index
+    return _check(lib().mla_default_num_parts(torch.cuda.current_device() if idx is None else idx))
 
 
 def num_items(B: int, H: int, T: int, topk: int = 0) -> int:
@@ -163,11 +163,45 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
     block_table int32 [B,max_pages]; cache_seqlens int32 [B]; topk_indices
     int32 [B,T,topk] or None.  tile_md/num_splits come from metadata() with
     the same arguments (computed here when omitted)."""
+    dev, B, T, H, fmt, topk = _decode_args(q, kv_cache, block_table, cache_seqlens, topk_indices, kv_scales)
+    if gathered is not None:
+        _need(gathered, "gathered", torch.int32, dev, 3)
+    if tile_md is None or num_splits is None:
+        tile_md, num_splits = metadata(cache_seqlens, H, T, topk=topk, causal=causal)
+    _need(tile_md, "tile_md", torch.int32, dev, 2)
+    _need(num_splits, "num_splits", torch.int32, dev, 1)
+    num_parts = tile_md.shape[0]
+    need = workspace_bytes(B, H, T, topk, num_parts)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", workspace.dtype, dev)
+    if out is None:
+        out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, 4)
+    _need(lse, "lse", torch.float32, dev, 3)
+    with torch.cuda.device(dev):
+        _check(lib().mla_decode(
+            _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1],
+            _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+            _ptr(topk_indices), topk, _ptr(gathered), _ptr(kv_scales),
+            float(softmax_scale), int(bool(causal)), _ptr(tile_md), _ptr(num_splits),
+            num_parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
+    return out, lse
+
+
+def _decode_args(q, kv_cache, block_table, cache_seqlens, topk_indices, kv_scales):
+    """Checks the decode inputs' dtypes, devices and shapes -> (device, B, T,
+    H, cache format, topk)."""
     _need(q, "q", torch.bfloat16, ndim=4)
     dev = q.device
     B, T, H, dq = q.shape
     if dq != D_QK:
         raise ValueError("q must be [B, T, H, 576]")
+    if not isinstance(kv_cache, torch.Tensor):
+        raise TypeError("kv_cache must be a torch.Tensor")
     if kv_cache.dtype == torch.bfloat16:
         fmt = KV_BF16
         if kv_cache.dim() != 3 or kv_cache.shape[2] != D_QK:
@@ -196,29 +230,7 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
         if tuple(topk_indices.shape[:2]) != (B, T):
             raise ValueError("topk_indices must be [B, T, topk]")
         topk = topk_indices.shape[2]
-    if gathered is not None:
-        _need(gathered, "gathered", torch.int32, dev, 3)
-    if tile_md is None or num_splits is None:
-        tile_md, num_splits = metadata(cache_seqlens, H, T, topk=topk, causal=causal)
-    num_parts = tile_md.shape[0]
-    need = workspace_bytes(B, H, T, topk, num_parts)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    if out is None:
-        out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
-    _need(out, "out", torch.bfloat16, dev, 4)
-    _need(lse, "lse", torch.float32, dev, 3)
-    with torch.cuda.device(dev):
-        _check(lib().mla_decode(
-            _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1],
-            _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
-            _ptr(topk_indices), topk, _ptr(gathered), _ptr(kv_scales),
-            float(softmax_scale), int(bool(causal)), _ptr(tile_md), _ptr(num_splits),
-            num_parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
-            _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
-    return out, lse
+    return dev, B, T, H, fmt, topk
 
 
 def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
@@ -229,18 +241,13 @@ def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.T
     """decode() for callers that cannot allocate device memory: schedule and
     workspace live in the library's fixed device scratch (mla_decode_noalloc).
     Only out / lse are created here when not given."""
-    _need(q, "q", torch.bfloat16, ndim=4)
-    dev = q.device
-    B, T, H, _ = q.shape
-    if kv_cache.dtype == torch.bfloat16:
-        fmt = KV_BF16
-    else:
-        fmt = KV_FP8_E4M3 if kv_cache.shape[2] == FP8_ROW_BYTES else KV_FP8_E4M3_TENSOR
-    topk = 0 if topk_indices is None else topk_indices.shape[2]
+    dev, B, T, H, fmt, topk = _decode_args(q, kv_cache, block_table, cache_seqlens, topk_indices, kv_scales)
     if out is None:
         out = torch.empty((B, T, H, D_V), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, 4)
+    _need(lse, "lse", torch.float32, dev, 3)
     with torch.cuda.device(dev):
         _check(lib().mla_decode_noalloc(
             _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
@@ -348,9 +355,11 @@ def query_absorb(q_a: torch.Tensor, w_qa: torch.Tensor, w_qb: torch.Tensor, w_uk
     need = query_absorb_workspace_bytes(N, H)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", workspace.dtype, dev)
     with torch.cuda.device(dev):
         _check(lib().mla_query_absorb(_ptr(q_a), ld, _ptr(w_qa), float(eps), _ptr(w_qb), _ptr(w_uk), N, H,
-                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream(dev)))
+                                      _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(dev)))
     return out
 
 
