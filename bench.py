@@ -170,14 +170,19 @@ def traffic_record(kernel_hash: str):
     return d
 
 
+# The sources the decode kernel is compiled from (its translation unit and
+# the headers it includes): the traffic record holds only while they are
+# unchanged.
+DECODE_KERNEL_SOURCES = ("common.cuh", "decode_tc.cu", "ptx.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_05_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()
 
 
