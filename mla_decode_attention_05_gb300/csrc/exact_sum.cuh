@@ -95,24 +95,52 @@ __device__ __noinline__ float sum_sq_wide(const LaneBf16<kWords> x, int emax) {
 // 1536 squares).  When emax >= 32 every zero lands below bit -32 and adds
 // nothing, so every value can take the normal significand 0x80 | mantissa.
 // A row with a nonzero value below the window (its exponent under emax - 31:
-// subnormals included) or with emax < 32 takes the wide form.  emax and the
-// smallest nonzero magnitude come from the 15-bit magnitude patterns, which
-// order like the values.
+// subnormals included) or with emax < 32 takes the wide form.  A row whose
+// nonzero values all lie within 2^15 of the largest (exponents emax - 15 ..
+// emax, the common case) puts every square into `hi` (s in [1, 31]) and
+// needs only that window.  emax and the smallest nonzero magnitude come from
+// the 15-bit magnitude patterns, which order like the values.
+// n * 2^e (n >= 1) rounded to fp32, ties to even: the correctly rounded
+// conversion of n, then e added to the exponent, which is exact while the
+// result is normal; a result that would be subnormal or zero takes the
+// general rounding (one rounding at the subnormal quantum).
+__device__ __forceinline__ float scaled_u64_to_f32(uint64_t n, int e) {
+  const uint32_t f = __float_as_uint(__ull2float_rn(n));
+  const int re = (int)(f >> 23) + e;  // biased exponent of the result
+  if (re >= 255) return __int_as_float(0x7F800000);
+  if (re >= 1) return __uint_as_float(f + ((uint32_t)e << 23));
+  return round_to_f32((unsigned __int128)n, e, false);
+}
+
 template <int kWords>
 __device__ __forceinline__ float sum_sq_rn(const LaneBf16<kWords> &x) {
-  uint32_t amax = 0, amin = 0x7FFFu;
+  // per 16-bit half: the largest magnitude, and the smallest of (magnitude -
+  // 1) over nonzero magnitudes (0x7FFF for a zero): with bit 15 set in both
+  // halves the subtraction of 1 never borrows across them
+  uint32_t amax2 = 0, aminm2 = 0xFFFFFFFFu;
 #pragma unroll
   for (int k = 0; k < kWords; k++) {
-    const uint32_t a0 = x.w[k] & 0x7FFFu, a1 = (x.w[k] >> 16) & 0x7FFFu;
-    amax = max(amax, max(a0, a1));
-    amin = min(amin, min(a0 ? a0 : 0x7FFFu, a1 ? a1 : 0x7FFFu));
+    amax2 = __vmaxu2(amax2, x.w[k] & 0x7FFF7FFFu);
+    aminm2 = __vminu2(aminm2, ((x.w[k] | 0x80008000u) - 0x00010001u) & 0x7FFF7FFFu);
   }
-  amax = __reduce_max_sync(0xffffffffu, amax);
+  const uint32_t amax = __reduce_max_sync(0xffffffffu, max(amax2 & 0xFFFFu, amax2 >> 16));
   if (amax == 0) return 0.f;  // all zeros
-  amin = __reduce_min_sync(0xffffffffu, amin);
+  const uint32_t amin = __reduce_min_sync(0xffffffffu, min(aminm2 & 0xFFFFu, aminm2 >> 16)) + 1u;
   const int emax = (int)(amax >> 7);
   if (emax < 32 || (int)(amin >> 7) < emax - 31) return sum_sq_wide<kWords>(x, max(emax, 1));
   const int base = 31 - 2 * emax;
+  if ((int)(amin >> 7) >= emax - 15) {
+    uint64_t hi = 0;
+#pragma unroll
+    for (int i = 0; i < 2 * kWords; i++) {
+      const uint32_t h = half_of(x, i);
+      const uint32_t m = (h & 0x7Fu) | 0x80u;
+      hi += (uint64_t)(m * m) * shl_or_zero(1u, 2 * (int)((h >> 7) & 0xFFu) + base);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hi += __shfl_xor_sync(0xffffffffu, (unsigned long long)hi, o);
+    return scaled_u64_to_f32(hi, 2 * emax - 299);  // hi > 0: the largest square is in it
+  }
   uint64_t hi = 0, lo = 0;
 #pragma unroll
   for (int i = 0; i < 2 * kWords; i++) {

@@ -80,13 +80,36 @@ __device__ __forceinline__ void issue_token(const KvInsertParams &p, int j, int 
   cp_async_commit();
 }
 
+// Tile scale s = max(fp32(amax / 448), 2^-126) and inv = fp32(1 / s) for a
+// bf16 amax > 0.  amax = m * 2^E with m its 8-bit significand (1..255), and
+// scaling by a power of two commutes with rounding while the result stays
+// normal, so s and inv are fp32(m / 448) and fp32(1 / fp32(m / 448)) (tables
+// built at kernel start with those same divisions) with E added to, or taken
+// from, the exponent.  A quotient below 2^-126 is the floor, whose
+// reciprocal is 2^126.
+__device__ __forceinline__ void tile_scale(float amax, const uint32_t *sc_tab, const uint32_t *inv_tab, float &sc,
+                                           float &inv) {
+  const uint32_t a = __float_as_uint(amax);
+  const int e = (int)((a >> 23) & 0xFFu);
+  const uint32_t m = ((a >> 16) & 0x7Fu) | (e ? 0x80u : 0u);
+  const int E = e ? e - 134 : -133;
+  const uint32_t sb = sc_tab[m];
+  if ((int)(sb >> 23) + E >= 1) {
+    sc = __uint_as_float(sb + ((uint32_t)E << 23));
+    inv = __uint_as_float(inv_tab[m] - ((uint32_t)E << 23));
+  } else {
+    sc = 0x1p-126f;
+    inv = 0x1p126f;
+  }
+}
+
 struct Token {
   uint4 xa, xb, pe;
   long long slot;
 };
 
 __device__ __forceinline__ void insert_token(const KvInsertParams &p, const Token &tk, const float (&w)[16],
-                                             int lane) {
+                                             int lane, const uint32_t *sc_tab, const uint32_t *inv_tab) {
   const long long slot = tk.slot;
   if (slot < 0 || slot >= p.n_slots) {
     if (slot != -1 && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
@@ -131,8 +154,8 @@ __device__ __forceinline__ void insert_token(const KvInsertParams &p, const Toke
     for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     // s = fp32(amax / 448), at least the smallest normal 2^-126 (so 1 / s
     // stays finite); 1 for an all-zero tile
-    const float sc = amax > 0.f ? fmaxf(__fdiv_rn(amax, 448.f), 0x1p-126f) : 1.f;
-    const float inv = __fdiv_rn(1.f, sc);
+    float sc = 1.f, inv = 1.f;
+    if (amax > 0.f) tile_scale(amax, sc_tab, inv_tab, sc, inv);
     uint32_t c[4];
 #pragma unroll
     for (int k = 0; k < 4; k++)
@@ -165,6 +188,14 @@ __device__ __forceinline__ void insert_token(const KvInsertParams &p, const Toke
 
 __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) kv_insert_kernel(KvInsertParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t sc_tab[256], inv_tab[256];  // fp32(m / 448), fp32(1 / that), m = 0..255
+  static_assert(kWarps * 32 == 256, "one table entry per thread");
+  {
+    const float q = __fdiv_rn((float)threadIdx.x, 448.f);
+    sc_tab[threadIdx.x] = __float_as_uint(q);
+    inv_tab[threadIdx.x] = __float_as_uint(__fdiv_rn(1.f, q));  // m = 0: unused
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int first = blockIdx.x * kWarps + warp;
   const int stride = gridDim.x * kWarps;
@@ -190,7 +221,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) kv_insert_kernel(Kv
     tk.pe = lane < 8 ? *reinterpret_cast<const uint4 *>(cur + 1024 + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
     tk.slot = *reinterpret_cast<const long long *>(cur + 1152);
     __syncwarp();  // every lane has read the stage before it is refilled
-    insert_token(p, tk, w, lane);
+    insert_token(p, tk, w, lane, sc_tab, inv_tab);
     st = st + 1 == kStages ? 0 : st + 1;
   }
   cp_async_wait<0>();
