@@ -30,7 +30,7 @@ namespace mla {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kBlocksPerSm = 3;
+constexpr int kBlocksPerSm = 4;
 
 template <int N>
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[N], int at) {
@@ -119,7 +119,7 @@ __device__ __forceinline__ void insert_token(const KvInsertParams &p, const Toke
   const uint32_t *xw = xr.w;
   const float S = sum_sq_rn<8>(xr);
   const float mean = __fadd_rn(__fmul_rn(S, 1.f / 512.f), p.eps);
-  const float r = mean > 0.f ? __fdiv_rn(1.f, __fsqrt_rn(mean)) : 0.f;
+  const float r = mean > 0.f ? __frcp_rn(__fsqrt_rn(mean)) : 0.f;
 
   // n_i = bf16(fp32(fp32(x_i * w_i) * r)), kept as packed bf16 pairs
   uint32_t nb[8];

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   const float S = sum_sq_rn<4 * kChunks>(x);
   const float mean = __fadd_rn(__fdiv_rn(S, (float)D_QA), eps);
-  const float r = mean > 0.f ? __fdiv_rn(1.f, __fsqrt_rn(mean)) : 0.f;
+  const float r = mean > 0.f ? __frcp_rn(__fsqrt_rn(mean)) : 0.f;
   uint4 *dst = reinterpret_cast<uint4 *>(xq + (size_t)j * D_QA);
 #pragma unroll
   for (int c = 0; c < kChunks; c++) {
