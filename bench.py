@@ -131,30 +131,38 @@ class Clocks:
         except Exception:
             self.proc.kill()
             out = ""
-        rows = []
-        for line in out.strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
-            except Exception:
-                continue
-        if not rows:
-            return {"samples": 0}
-        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
-        used = inside if inside else [min(rows, key=lambda r: abs(r[0] - (self.t0 or r[0])))]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for r in used:
-            for n, v in zip(names, r[3][1:5]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
-                "reasons": sorted(reasons), "samples": len(used),
-                "in_timed_region": bool(inside)}
+        return summarise_clocks(out, self.t0, self.t1)
+
+
+def summarise_clocks(text: str, t0, t1) -> dict:
+    """The `clocks` entry from nvidia-smi CSV rows (Clocks.FIELDS, no header,
+    no units): median and maximum SM clock and the throttle reasons seen
+    during [t0, t1] (local time, 50 ms of slack), or the sample nearest t0
+    when none falls inside."""
+    rows = []
+    for line in text.strip().splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+        except Exception:
+            continue
+    if not rows:
+        return {"samples": 0}
+    inside = [r for r in rows if t0 is not None and t0 - 0.05 <= r[0] <= t1 + 0.05]
+    used = inside if inside else [min(rows, key=lambda r: abs(r[0] - (t0 or r[0])))]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    for r in used:
+        for n, v in zip(names, r[3][1:5]):
+            if v.strip().lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+            "reasons": sorted(reasons), "samples": len(used),
+            "in_timed_region": bool(inside)}
 
 
 def traffic_record(kernel_hash: str):
