@@ -21,10 +21,19 @@
  * block_table[b][n / 64], slot n % 64 (vLLM MlaQuery.insert: page, offset =
  * slot // page_size, slot % page_size).
  *
- * Ownership: the caller owns every buffer; the library allocates no device or
- * host memory of its own on these paths (a small host-side cache of TMA
- * descriptors aside).  Every call is asynchronous on `stream` and never
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory of its own, with two exceptions: mla_query_absorb creates a cuBLAS
+ * handle (which allocates cuBLAS's workspace) at its first call on each
+ * thread and device, and mla_decode_noalloc keeps one fixed scratch array per
+ * device.  TMA tensor maps are encoded on the host at each call and passed as
+ * kernel parameters.  Every call is asynchronous on `stream` and never
  * synchronises the host, except mla_device_status().
+ *
+ * CUDA graphs: every call can be captured into a CUDA graph on `stream` once
+ * the calling thread has made the same kind of call outside capture (the
+ * first call does one-time host set-up).  A replay uses the buffers seen at
+ * capture and reads their contents at replay time; the split-KV schedule is
+ * a device kernel, so it follows the sequence lengths of each replay.
  *
  * Errors: each call returns MLA_OK (0) or a negative code; the text of the
  * last error of the calling thread is kept for mla_last_error_string().
@@ -245,8 +254,8 @@ int mla_decode_noalloc(const void *q, const void *kv_cache, int kv_format,
  *                            rows, value = e4m3 * scale)
  *   MLA_KV_FP8_E4M3_TENSOR:  e4m3(fp32(n_i * k_scale_inv)), e4m3(fp32(pe_i *
  *                            k_scale_inv)) (576 bytes; the per-tensor
- *                            FP8 layout; written only, mla_decode does not
- *                            read it)
+ *                            FP8 layout; mla_decode reads it with the one
+ *                            scale 1 / k_scale_inv)
  * e4m3 = OCP FP8 E4M3, round to nearest even, saturated to +-448.  The sum
  * of squares is taken as integers (a bf16 square is an 8-bit integer squared
  * times a power of two), so the written bytes are a function of the inputs
