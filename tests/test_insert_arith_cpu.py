@@ -97,3 +97,26 @@ def test_one_window_sum_of_squares_matches_exact_rounding():
         want = K.fraction_to_f32(K.exact_sum_sq(K.bf16_bits_to_f64(r)))
         assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32)
     assert taken > 300
+
+
+def test_packed_smallest_nonzero_magnitude():
+    """3. The range check reads two bf16 values per 32-bit word: with bit 15
+    set in both halves, subtracting 0x00010001 never borrows across them, so
+    per half ((w | 0x80008000) - 0x00010001) & 0x7FFF7FFF is magnitude - 1
+    for a nonzero value and 0x7FFF for a zero; the minimum over the row plus
+    one is the smallest nonzero magnitude (0x8000 when every value is zero)."""
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        n = 16
+        halves = rng.integers(0, 1 << 16, size=2 * n, dtype=np.uint32)
+        halves[rng.random(2 * n) < 0.3] &= 0x8000          # zeros of either sign
+        if trial % 50 == 0:
+            halves &= 0x8000                                 # an all-zero row
+        words = halves[0::2] | (halves[1::2] << 16)
+        t = (((words | 0x80008000) - 0x00010001) & 0x7FFF7FFF).astype(np.uint32)
+        got = int(min((t & 0xFFFF).min(), (t >> 16).min())) + 1
+        mags = halves & 0x7FFF
+        want = int(mags[mags != 0].min()) if (mags != 0).any() else 0x8000
+        assert got == want
+        amax = int(max(((words & 0x7FFF7FFF) & 0xFFFF).max(), ((words & 0x7FFF7FFF) >> 16).max()))
+        assert amax == int(mags.max())
