@@ -1,4 +1,4 @@
-"""Two arithmetic shortcuts of the KV insert kernel, checked on the CPU.
+"""Three arithmetic shortcuts of the KV insert kernel, checked on the CPU.
 
 1. FP8 tile scales.  For a tile maximum amax (a bf16 value m * 2^E, m its
    8-bit significand) the kernel takes s = max(fp32(amax / 448), 2^-126) and
@@ -14,6 +14,9 @@
    result is normal, else one rounding at the subnormal quantum).  Restated
    here in integer steps and compared with the oracle's exact sum
    (oracle/kv_insert.py) on rows scaled across the whole fp32 range.
+
+3. The packed range check that picks the branch: the largest and the
+   smallest nonzero magnitude of a row, two bf16 values per 32-bit word.
 """
 import os
 import sys
@@ -100,7 +103,7 @@ def test_one_window_sum_of_squares_matches_exact_rounding():
 
 
 def test_packed_smallest_nonzero_magnitude():
-    """3. The range check reads two bf16 values per 32-bit word: with bit 15
+    """The range check reads two bf16 values per 32-bit word: with bit 15
     set in both halves, subtracting 0x00010001 never borrows across them, so
     per half ((w | 0x80008000) - 0x00010001) & 0x7FFF7FFF is magnitude - 1
     for a nonzero value and 0x7FFF for a zero; the minimum over the row plus
