@@ -194,6 +194,33 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def device_l2_bytes(local: int) -> int:
+    """L2 size of the device (the nominal GB300 figure if torch does not
+    report it)."""
+    try:
+        import torch
+        n = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0))
+        return n if n > 0 else L2_BYTES
+    except Exception:
+        return L2_BYTES
+
+
+def step_bytes(w, kv_bytes: int) -> int:
+    """Bytes one decode step touches in memory: the KV rows it reads (each
+    distinct row once), the query rows, and the output and LSE it writes."""
+    rows = w.B * w.T * w.H
+    return int(kv_bytes) + rows * 576 * 2 + rows * 512 * 2 + rows * 4
+
+
+def l2_label(touched: int, l2_bytes: int, flushed: bool) -> str:
+    """The `config.l2` entry: what a step touches against the L2, and whether
+    the L2 was flushed between timed steps."""
+    head = f"{touched / 1e6:.1f} MB touched per step vs {l2_bytes / 1e6:.1f} MB L2"
+    if flushed:
+        return head + f"; L2 flushed before every timed step ({2 * l2_bytes / 1e6:.0f} MB written, outside the timed events)"
+    return head + "; inputs larger than twice the L2, no flush"
+
+
 def subset(w, nb: int):
     """The first nb sequences of a workload (the page pool is kept whole)."""
     import dataclasses
@@ -253,7 +280,7 @@ def cpu_baseline(w, budget_s: float = 12.0):
             "tflops": fl / dt / 1e12}
 
 
-def run_gpu(args, w, world, rank, local):
+def run_gpu(args, w, world, rank, local, l2_bytes):
     import torch
     import mla_decode_attention_05_gb300 as mla
     dev = torch.device("cuda", local)
@@ -305,13 +332,19 @@ def run_gpu(args, w, world, rank, local):
             raise RuntimeError(L.mla_last_error_string().decode())
 
     launches_per_step = 3  # metadata, decode, combine
+    # A step that touches less than twice the L2 would find its inputs in L2
+    # from the step before: write a buffer of twice the L2 before each such
+    # timed step (outside the timed events) so that they come from HBM.
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     for _ in range(args.warmup):
         step(q, kv, bt, sk, sc, tk, out, lse)
     torch.cuda.synchronize()
     K = args.steps
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for e in ev_b + ev_a:   # create the underlying events before handing them over
+    st_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    st_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_b + ev_a + st_b + st_a:   # create the underlying events before handing them over
         e.record(stream)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -320,14 +353,22 @@ def run_gpu(args, w, world, rank, local):
     if clocks:
         clocks.mark_start()
     # 1. the steps as a user runs them: nothing between the three kernels
+    #    (with the L2 flush: events around each step, the flush between)
     start.record(stream)
     for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+            st_b[i].record(stream)
         step(q, kv, bt, sk, sc, tk, out, lse)
+        if flush is not None:
+            st_a[i].record(stream)
     end.record(stream)
     # 2. the same steps with events around each decode kernel (an event
     #    between two kernels stops the second one from starting early, so
     #    this loop only serves the kernel's own duration)
     for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
         mla.profile_events(ev_b[i], ev_a[i])
         step(q, kv, bt, sk, sc, tk, out, lse)
     mla.profile_events()
@@ -335,7 +376,10 @@ def run_gpu(args, w, world, rank, local):
     if clocks:
         clocks.mark_end()
     barrier(world)
-    total_ms = start.elapsed_time(end)
+    if flush is not None:
+        total_ms = sum(b.elapsed_time(a) for b, a in zip(st_b, st_a))
+    else:
+        total_ms = start.elapsed_time(end)
     kern_ms = [b.elapsed_time(a) for b, a in zip(ev_b, ev_a)]
     status = mla.device_status()
     clk = clocks.finish() if clocks else None
@@ -618,7 +662,7 @@ def run_query(args, world, rank, local, hbm, peak_src):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights of the layer's shapes)",
         "config": {"workload": f"query_absorb_n{N}_h{H}", "tokens": N, "H": H, "bytes": nbytes,
                    "l2": "256 MB written before every timed call (weights 92 MB would otherwise stay in L2)",
-                   "gemms": "cuBLAS (bf16, fp32 accumulate): Q_B and the per-head W_UK",
+                   "gemms": "Q_B: cuBLAS (bf16, fp32 accumulate); W_UK: this library's tcgen05 kernel",
                    "parallelism": f"weak, {world} independent replica(s)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "traffic": None, "kernel_ms": step_ms,
@@ -723,7 +767,10 @@ def main():
     if args.batch:
         w = subset(w, args.batch)
     kv_bytes, flops = work_of(w)
-    r = run_gpu(args, w, world, rank, local)
+    l2_bytes = device_l2_bytes(local)
+    touched = step_bytes(w, kv_bytes)
+    args.flush_l2 = touched < 2 * l2_bytes
+    r = run_gpu(args, w, world, rank, local, l2_bytes)
     step_ms = max_over_ranks(r["total_ms"] / args.steps, world)
     kern_ms = statistics.mean(r["kern_ms"])
     kern_ms_max = max_over_ranks(kern_ms, world)
@@ -755,7 +802,7 @@ def main():
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "kv_format": "bf16" if w.kv_format == 0 else "fp8_e4m3",
                    "causal": w.causal, "topk": w.topk_len, "page_size": 64, "num_parts": r["parts"],
                    "kv_bytes": kv_bytes, "flops": flops, "seed": w.seed,
-                   "l2": f"inputs larger than L2 ({w.kv.nbytes / 1e9:.2f} GB cache vs {L2_BYTES / 1e6:.0f} MB L2); no flush",
+                   "l2": l2_label(touched, l2_bytes, args.flush_l2),
                    "parallelism": f"weak, {world} independent replica(s)",
                    "kernel_timing": f"decode kernel duration from a second {args.steps}-step loop with CUDA events around each decode launch"},
         "roofline": roof,

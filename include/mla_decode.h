@@ -16,7 +16,7 @@
  *
  * where N(b,t) = {n < s_k}                       dense
  *               {n < s_k - T + t + 1}           causal (query token t of T)
- *               {topk[b,t,j] : j, != -1}        sparse top-k
+ *               {topk[b,t,j] : j, != -1}        sparse top-k (distinct)
  * and K_n is the cache row of logical token n of sequence b, found at page
  * block_table[b][n / 64], slot n % 64 (vLLM MlaQuery.insert: page, offset =
  * slot // page_size, slot % page_size).
@@ -29,9 +29,10 @@
  * kernel parameters.  Every call is asynchronous on `stream` and never
  * synchronises the host, except mla_device_status().
  *
- * CUDA graphs: every call can be captured into a CUDA graph on `stream` once
- * the calling thread has made the same kind of call outside capture (the
- * first call does one-time host set-up).  A replay uses the buffers seen at
+ * CUDA graphs: mla_decode_metadata, mla_decode, mla_kv_insert and
+ * mla_query_absorb can be captured into a CUDA graph on `stream` once the
+ * calling thread has made the same kind of call outside capture (the first
+ * call does one-time host set-up).  A replay uses the buffers seen at
  * capture and reads their contents at replay time; the split-KV schedule is
  * a device kernel, so it follows the sequence lengths of each replay.
  *
@@ -70,6 +71,8 @@ extern "C" {
 #define MLA_STATUS_BAD_TOPK 2u      /* top-k index >= s_k or < -1               */
 #define MLA_STATUS_BAD_SEQLEN 4u    /* negative s_k, or more pages than max_pages */
 #define MLA_STATUS_WAIT_TIMEOUT 8u  /* a bounded device wait gave up            */
+#define MLA_STATUS_SMEM_ALIGN 16u   /* dynamic shared memory not 1024-byte aligned:
+                                       the decode kernel did nothing */
 
 /* Limits of this library. */
 #define MLA_PAGE_SIZE 64
@@ -151,7 +154,12 @@ size_t mla_decode_workspace_bytes(int B, int H, int T, int topk, int num_parts);
  *   block_table    device int32 [B][max_pages]: page of the j-th 64 tokens
  *   cache_seqlens  device int32 [B]: s_k per sequence
  *   topk_indices   device int32 [B][T][topk] or NULL: token positions within
- *                  the sequence, -1 = unused slot; requires causal == 0
+ *                  the sequence, -1 = unused slot; requires causal == 0.
+ *                  The positions of one (b, t) list must be distinct (a
+ *                  top-k selection names each cache token at most once;
+ *                  -1 may repeat).  This is a precondition, not checked: a
+ *                  position listed twice would be loaded and weighted twice,
+ *                  which is not the attention defined above.
  *   gathered       device int32 [B][T][topk] or NULL (top-k only): if given,
  *                  the kernel writes, per slot, the token position whose row
  *                  it loaded, or -1 for a slot it skipped
@@ -209,10 +217,14 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
  * workers, and allocates nothing: no cudaMalloc, no cudaFree, no allocating
  * library call.
  *
- *   Limits: requests whose schedule + workspace would exceed the scratch (on a
- *   152-SM GB300 that is more than about 160 work items, e.g. B > ~160 for
- *   T = 1, H = 128) return MLA_ERR_WORKSPACE, with the byte counts in
- *   mla_last_error_string(); use mla_decode for those.
+ *   Limits: a request fits when its schedule (num_parts * 32 bytes and
+ *   (num_items + 1) * 4 bytes, each rounded up to 256) plus
+ *   mla_decode_workspace_bytes(B, H, T, topk, num_parts) is at most
+ *   MLA_NOALLOC_SCRATCH_BYTES, with num_parts = mla_default_num_parts(device).
+ *   On a 152-SM GB300 (76 workers) that is at most 138 work items: B <= 138
+ *   at T * H <= 128, B <= 69 at T * H = 256.  Larger requests return
+ *   MLA_ERR_WORKSPACE, with the byte counts in mla_last_error_string(), and
+ *   enqueue nothing; use mla_decode for those.
  *   Set-up: the first call on a device, with that device current, looks up
  *   the scratch's device address (cudaGetSymbolAddress); make that first call
  *   before any stream capture.
@@ -336,6 +348,20 @@ int mla_device_status(uint32_t *status);
  * is outside).  Pass NULL, NULL to stop.  Returns MLA_OK.
  */
 int mla_profile_events(void *before, void *after);
+
+/*
+ * Test hook for the failure path: the time limit, in nanoseconds, of every
+ * bounded wait inside the decode kernel of later mla_decode and
+ * mla_decode_noalloc calls made on the calling thread (0 restores the
+ * default of 2 s).  A wait that runs out sets MLA_STATUS_WAIT_TIMEOUT; every
+ * role of the kernel then gives up at its next wait, the kernel waits for
+ * its own copies and MMAs in flight, frees its tensor memory and returns, and
+ * the context stays usable.  The out and lse of such a call are undefined.
+ * With a limit of a few microseconds, real waits of an ordinary call run
+ * out, so a test can exercise this path without faulting or hanging the GPU.
+ * Not meant for production calls.  Returns MLA_OK.
+ */
+int mla_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -38,6 +38,7 @@ STATUS_BAD_PAGE = 1
 STATUS_BAD_TOPK = 2
 STATUS_BAD_SEQLEN = 4
 STATUS_WAIT_TIMEOUT = 8
+STATUS_SMEM_ALIGN = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,7 @@ def lib():
             L.mla_last_error_string.restype = ctypes.c_char_p
             L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.mla_profile_events.argtypes = [P, P]
+            L.mla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             _lib = L
     return _lib
 
@@ -181,6 +183,11 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
         lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     _need(out, "out", torch.bfloat16, dev, 4)
     _need(lse, "lse", torch.float32, dev, 3)
+    check_decode_shapes(B, T, H, topk, kv_cache.shape[0], out_shape=out.shape, lse_shape=lse.shape,
+                        kv_scales_shape=kv_scales.shape if fmt == KV_FP8_E4M3 else None,
+                        tile_md_shape=tile_md.shape, num_splits_numel=num_splits.numel(),
+                        n_items=num_items(B, H, T, topk),
+                        gathered_shape=None if gathered is None else gathered.shape)
     with torch.cuda.device(dev):
         _check(lib().mla_decode(
             _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1],
@@ -190,6 +197,30 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
             num_parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
             _ptr(out), _ptr(lse), B, T, H, _stream(dev)))
     return out, lse
+
+
+def check_decode_shapes(B: int, T: int, H: int, topk: int, num_pages: int, *,
+                        out_shape, lse_shape, kv_scales_shape=None, tile_md_shape=None,
+                        num_splits_numel=None, n_items=None, gathered_shape=None) -> None:
+    """Shape checks of the caller-given decode buffers (the C ABI sees only
+    pointers, so a buffer that is too small would be written past its end):
+    out [B,T,H,512], lse [B,H,T], per-128 FP8 scales [num_pages,64,4],
+    tile_md [parts,8], num_splits with at least n_items + 1 entries, and a
+    gathered record shaped like the top-k indices [B,T,topk].  Raises
+    ValueError."""
+    if tuple(out_shape) != (B, T, H, D_V):
+        raise ValueError(f"out must be [{B}, {T}, {H}, {D_V}], got {list(out_shape)}")
+    if tuple(lse_shape) != (B, H, T):
+        raise ValueError(f"lse must be [{B}, {H}, {T}], got {list(lse_shape)}")
+    if kv_scales_shape is not None and tuple(kv_scales_shape) != (num_pages, PAGE_SIZE, 4):
+        raise ValueError(f"kv_scales must be [{num_pages}, {PAGE_SIZE}, 4], got {list(kv_scales_shape)}")
+    if tile_md_shape is not None:
+        if len(tile_md_shape) != 2 or tile_md_shape[1] != 8 or tile_md_shape[0] < 1:
+            raise ValueError(f"tile_md must be [num_parts, 8], got {list(tile_md_shape)}")
+    if num_splits_numel is not None and (n_items is None or num_splits_numel < n_items + 1):
+        raise ValueError(f"num_splits needs {n_items} + 1 entries, got {num_splits_numel}")
+    if gathered_shape is not None and tuple(gathered_shape) != (B, T, topk):
+        raise ValueError(f"gathered must be [{B}, {T}, {topk}], got {list(gathered_shape)}")
 
 
 def _decode_args(q, kv_cache, block_table, cache_seqlens, topk_indices, kv_scales):
@@ -248,6 +279,8 @@ def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.T
         lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     _need(out, "out", torch.bfloat16, dev, 4)
     _need(lse, "lse", torch.float32, dev, 3)
+    check_decode_shapes(B, T, H, topk, kv_cache.shape[0], out_shape=out.shape, lse_shape=lse.shape,
+                        kv_scales_shape=kv_scales.shape if fmt == KV_FP8_E4M3 else None)
     with torch.cuda.device(dev):
         _check(lib().mla_decode_noalloc(
             _ptr(q), _ptr(kv_cache), fmt, kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
@@ -368,6 +401,13 @@ def device_status() -> int:
     v = ctypes.c_uint32()
     _check(lib().mla_device_status(ctypes.byref(v)))
     return int(v.value)
+
+
+def set_wait_limit_ns(ns: int = 0):
+    """Test hook: the limit of the decode kernel's bounded waits for later
+    decode calls on this thread (0 = the default, 2 s); see
+    mla_set_wait_limit_ns in include/mla_decode.h."""
+    _check(lib().mla_set_wait_limit_ns(int(ns)))
 
 
 def profile_events(before=None, after=None):

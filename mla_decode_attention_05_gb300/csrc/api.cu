@@ -18,6 +18,7 @@ namespace {
 thread_local char g_err[512] = "";
 thread_local cudaEvent_t g_ev_before = nullptr;
 thread_local cudaEvent_t g_ev_after = nullptr;
+thread_local unsigned long long g_wait_ns = mla::kDefaultWaitNs;
 
 int fail(int code, const char *fmt, ...) {
   va_list ap;
@@ -229,6 +230,7 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   p.num_parts = num_parts;
   p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.scale_log2 = softmax_scale * mla::LOG2E;
+  p.wait_ns = g_wait_ns;
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = mla::launch_decode(p, s, g_ev_before, g_ev_after);
@@ -293,6 +295,11 @@ int mla_device_status(uint32_t *status) {
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_mla_status, &zero, sizeof zero);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   *status = v;
+  return ok();
+}
+
+int mla_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns = ns == 0 ? mla::kDefaultWaitNs : (unsigned long long)ns;
   return ok();
 }
 

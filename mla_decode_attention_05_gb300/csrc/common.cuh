@@ -52,7 +52,11 @@ struct DecodeParams {
   int num_parts;
   int out_v8;        // out is 32-byte aligned: 32-byte stores
   float scale_log2;  // softmax_scale * log2(e)
+  unsigned long long wait_ns;  // limit of every bounded device wait
 };
+
+// Default limit of the decode kernel's bounded waits.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // Geometry of one work item.
 struct Item {

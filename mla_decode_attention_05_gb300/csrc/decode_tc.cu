@@ -66,7 +66,6 @@ constexpr int kSlotBytes = kPBytes + kMetaBytes;  // one P message (P_SLOT_BYTES
 static_assert(kSlotBytes <= P_SLOT_BYTES, "P ring slot");
 constexpr int kMaskRing = 8;
 constexpr int kPublishBatch = 4;                  // P messages published per fence, at most
-constexpr uint64_t kWaitNs = 2000000000ull;       // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // shared memory map (byte offsets from a 1024-aligned base)
@@ -125,17 +124,29 @@ struct Ctx {
 };
 
 __device__ __forceinline__ bool wait_or_abort(const Ctx &c, uint64_t *bar, uint32_t parity) {
-  if (mbar_wait<false>(smem_u32(bar), parity, &c.bars->abort, kWaitNs)) return true;
+  if (mbar_wait<false>(smem_u32(bar), parity, &c.bars->abort, c.p->wait_ns)) return true;
   atomicOr(c.p->status, MLA_STATUS_WAIT_TIMEOUT);
   c.bars->abort = 1;
   return false;
 }
 
 __device__ __forceinline__ bool wait_cluster_or_abort(const Ctx &c, uint64_t *bar, uint32_t parity) {
-  if (mbar_wait<true>(smem_u32(bar), parity, &c.bars->abort, kWaitNs)) return true;
+  if (mbar_wait<true>(smem_u32(bar), parity, &c.bars->abort, c.p->wait_ns)) return true;
   atomicOr(c.p->status, MLA_STATUS_WAIT_TIMEOUT);
   c.bars->abort = 1;
   return false;
+}
+
+// Whole-warp forms for the softmax and epilogue warps, whose lanes go on to
+// warp-collective tcgen05 loads and stores: every lane returns the same
+// answer (false if any lane's wait gave up), so a warp never splits between
+// giving up and going on.  `need` false: this lane only votes.
+__device__ __forceinline__ bool warp_wait(const Ctx &c, uint64_t *bar, uint32_t parity, bool need = true) {
+  return __all_sync(0xffffffffu, !need || wait_or_abort(c, bar, parity));
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(const Ctx &c, uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_cluster_or_abort(c, bar, parity));
 }
 
 // Walk the pieces of this worker: f(item_index, item, t0, t1, piece, empty).
@@ -440,12 +451,14 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   }
   const uint32_t rowbytes = rope ? fp8_row_bytes(p) : 512;
   const uint32_t raw = st + pi * rowbytes;
-  if (!wait_or_abort(c, raw_bar, raw_par)) return false;
+  // A thread whose wait gives up skips the work but still meets the other
+  // gather threads at the barrier below, so all 128 leave together.
+  const bool landed = wait_or_abort(c, raw_bar, raw_par);
   // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them (half 0:
   // 5, 6; half 1: 7 and the RoPE block); rank 1: bytes 0..32767, blocks 4-7
   // lie past them (half 0: 4, 5; half 1: 6, 7)
   const int split = rope ? 5 : 4;
-  const int hi0 = split + 2 * half, hi1 = half ? 8 : split + 2;
+  const int hi0 = split + 2 * half, hi1 = landed ? (half ? 8 : split + 2) : hi0;
   for (int kb = hi0; kb < hi1; kb++)
 #pragma unroll
     for (int u = 0; u < 4; u++) {
@@ -454,7 +467,7 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
-  if (rope && half == 1) {
+  if (landed && rope && half == 1) {
     if (p.kv_format == MLA_KV_FP8_E4M3_TENSOR) {  // 64 e4m3 RoPE values x the scale
 #pragma unroll
       for (int u = 0; u < 4; u++) {
@@ -471,12 +484,13 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   // blocks below the staging area: half 0 takes blocks [0, lo_split), half
   // 1 [lo_split, split) (rank 0: 0-2 | 3-4; rank 1: 0-1 | 2-3)
   const int lo_split = rope ? 3 : 2;
-  const int lo0 = half ? lo_split : 0, lo1 = half ? split : lo_split;
+  const int lo0 = half ? lo_split : 0, lo1 = landed ? (half ? split : lo_split) : lo0;
   uint4 v[12];  // e4m3 bytes of this thread's blocks below the staging area (at most 3 x 64 bytes)
 #pragma unroll
   for (int u = 0; u < 12; u++)
     if (u < (lo1 - lo0) * 4) v[u] = ld_shared_v4(raw + lo0 * 64 + u * 16);
-  named_bar_sync(kGatherBar, kGatherThreads);  // every staged byte below the blocks has been read
+  // every staged byte below the blocks has been read (or some thread gave up)
+  if (bar_red_or(kGatherBar, kGatherThreads, !landed)) return false;
 #pragma unroll
   for (int u = 0; u < 12; u++) {
     if (u >= (lo1 - lo0) * 4) break;
@@ -872,7 +886,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     }
     {  // the query rows, from the stage ring into TMEM
       const uint32_t qs = sq + (r >> 6);  // rows past the item (ri.ok false) read nothing
-      if (ri.ok && !wait_or_abort(c, &br.kv_full[qs % 3], (qs / 3) & 1)) return false;
+      if (!warp_wait(c, &br.kv_full[qs % 3], (qs / 3) & 1, ri.ok)) return false;
       load_q(lt, kv0 + (qs % 3) * kStage0Bytes, r & 63, ri.ok, hf ? 5 : 0, hf ? 9 : 5);
       sq += q_stages(it) + (t1 - t0);
     }
@@ -887,7 +901,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     for (int tile = t0; tile < t1; tile++, g++) {
       const uint32_t b = g & 1, u = g >> 1, mi = g % kMaskRing;
       // 1. tile validity and this row's 64 scores
-      if (!wait_or_abort(c, &br.mfull[mi], (g / kMaskRing) & 1)) return false;
+      if (!warp_wait(c, &br.mfull[mi], (g / kMaskRing) & 1)) return false;
       uint32_t mlo = br.mask[mi][0], mhi = br.mask[mi][1];
       const int lim = my_len - tile * PAGE;
       if (lim < 64) {
@@ -895,7 +909,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
         mlo &= (uint32_t)keep;
         mhi &= (uint32_t)(keep >> 32);
       }
-      if (!wait_or_abort(c, &br.s_full[b], u & 1)) return false;
+      if (!warp_wait(c, &br.s_full[b], u & 1)) return false;
       tc_fence_after();
       float own[32], oth[32];  // this half's 32 scores and the partner half's
       tmem_ld32(lt + TM_S + b * 64 + hf * 32, *reinterpret_cast<uint32_t(*)[32]>(&own[0]));
@@ -925,7 +939,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       // 4. P = 2^(s*c - m_ref*c) for this half's 32 tokens -> bf16 into ring
       //    slot g % P_RING, chunk-major (chunk ch of row r at ch*2048 + r*16)
       const uint32_t gs = g % P_RING;
-      if (!wait_cluster_or_abort(c, &br.gfree[gs], ((g / P_RING) & 1) ^ 1)) return false;
+      if (!warp_wait_cluster(c, &br.gfree[gs], ((g / P_RING) & 1) ^ 1)) return false;
       uint8_t *slot = p.ws_p + ((size_t)c.part * P_RING + gs) * P_SLOT_BYTES;
       float psum = 0.f;
 #pragma unroll
@@ -951,7 +965,7 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
         lp[hf * M_TILE + r] = l;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&br.lsum[q][pc & 1]));
-        if (!wait_or_abort(c, &br.lsum[q][pc & 1], (pc >> 1) & 1)) return false;
+        if (!warp_wait(c, &br.lsum[q][pc & 1], (pc >> 1) & 1)) return false;
         l_all = lp[r] + lp[M_TILE + r];
         if (hf == 0) mo->ell[r] = l_all;
       }
@@ -1032,7 +1046,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       //    so the L2 latency overlaps PV(g-2).  The bulk-copy engine would
       //    queue it behind this SM's V loads.  .cg: the slot was rewritten by
       //    another SM since this SM last read it.
-      if (!wait_cluster_or_abort(c, &br.p_full[gs], (g / P_RING) & 1)) return false;
+      if (!warp_wait_cluster(c, &br.p_full[gs], (g / P_RING) & 1)) return false;
       const uint8_t *slot = ring_slot(p, c.part, g);
       const uint4 *src = reinterpret_cast<const uint4 *>(slot);
       uint4 v[4];
@@ -1044,7 +1058,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       const float alpha = __ldcg(&m->alpha[r]);
       if (tile == t1 - 1) ell = __ldcg(&m->ell[r]);
       // 2. shared buffer b is free once PV(g-2) is done
-      if (!wait_or_abort(c, &br.p_empty[b], (u & 1) ^ 1)) return false;
+      if (!warp_wait(c, &br.p_empty[b], (u & 1) ^ 1)) return false;
 #pragma unroll
       for (int k = 0; k < 4; k++) st_shared_v4(pbuf + b * kPBytes + (e + 256 * k) * 16, v[k]);
       // The slot goes back to rank 0 once this warp's loads are done: the P
@@ -1065,7 +1079,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       }
       const uint32_t fl = f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w;
       if (fl != 0u) {  // rare: O *= alpha after PV(g-1), before PV(g)
-        if (!wait_or_abort(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
+        if (!warp_wait(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
         tc_fence_after();
         for (int cc = 0; cc < 8; cc++) {
           uint32_t o[32];
@@ -1083,7 +1097,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     }
     // O / l for the final output, or the normalised split partial (the
     // commit after the last PV covers every earlier MMA)
-    if (!wait_or_abort(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
+    if (!warp_wait(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
     tc_fence_after();
     const float inv = ell > 0.f ? 1.f / ell : 0.f;
     float *wrow = p.ws_o + (ri.slot * M_TILE + r) * D_V + hf * 256;
@@ -1126,7 +1140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
                      const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the shared-memory map needs a 1024-aligned base
-    if (threadIdx.x == 0) atomicOr(p.status, MLA_STATUS_WAIT_TIMEOUT);
+    if (threadIdx.x == 0) atomicOr(p.status, MLA_STATUS_SMEM_ALIGN);
     return;
   }
   uint8_t *base = smem_raw;

@@ -100,6 +100,9 @@ def valid_keys(w, b: int, t: int) -> np.ndarray:
     out = np.empty(cap, dtype=np.int32)
     n = lib.oracle_valid_keys(b, t, w.T, _ptr(sk), _ptr(tk), w.topk_len,
                               int(w.causal), _ptr(out), cap)
+    if n == -2:
+        raise ValueError(f"oracle: the top-k list of (b={b}, t={t}) repeats a position "
+                         "(the indices of one query token must be distinct)")
     return out[:n].copy()
 
 
@@ -121,6 +124,9 @@ def decode_rows(w, rows) -> tuple:
         int(kv.shape[1]), _ptr(sc), _ptr(bt), w.max_pages, _ptr(sk), _ptr(tk),
         w.topk_len, float(w.softmax_scale), int(w.causal), _ptr(rows), n,
         _ptr(out), _ptr(lse))
+    if rc == -2:
+        raise ValueError("oracle: a top-k list repeats a position "
+                         "(the indices of one query token must be distinct)")
     if rc != 0:
         raise ValueError("oracle: bad row or page index")
     return out, lse

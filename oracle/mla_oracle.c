@@ -20,6 +20,8 @@
  *           query token t of T sees the keys up to its own position), or the
  *           top-k indices of (b, t) other than -1 (sparse; FlashMLA issue #169
  *           is the sparse decode kernel, whose mask step drops invalid slots).
+ *           The indices of one list are distinct positions (a list that
+ *           repeats one is refused: see oracle_valid_keys).
  *   s_n   = softmax_scale * sum_d q_d K_{n,d}           (d over all 576)
  *   LSE   = m + ln(sum_{n in N} exp(s_n - m)),  m = max_n s_n
  *   O     = sum_{n in N} exp(s_n - LSE) V_n
@@ -113,7 +115,11 @@ static int load_key_row(const oracle_cache *c, int b, int n, double *row)
 }
 
 /* The valid key set of query token t of sequence b, sorted ascending.
- * Writes at most cap entries; returns the set's size. */
+ * Writes at most cap entries; returns the set's size, or -2 when a top-k
+ * list names one position twice: the indices of one query token are a
+ * selection of distinct cache positions (top-k of a score over the tokens,
+ * FlashMLA issue #169's sparse decode), so a repeated position is outside
+ * the definition and the oracle refuses it rather than pick a meaning. */
 int oracle_valid_keys(int b, int t, int T, const int32_t *cache_seqlens,
                       const int32_t *topk, int topk_len, int causal,
                       int32_t *out, int cap)
@@ -122,12 +128,16 @@ int oracle_valid_keys(int b, int t, int T, const int32_t *cache_seqlens,
     int count = 0;
     if (topk != NULL && topk_len > 0) {
         const int32_t *ids = topk + ((int64_t)b * T + t) * topk_len;
-        /* membership by scanning the key positions in order: sorted, and a
-         * repeated index would count once */
+        /* membership by scanning the key positions in order (sorted) */
         char *seen = (char *)calloc((size_t)(sk > 0 ? sk : 1), 1);
         for (int k = 0; k < topk_len; k++)
-            if (ids[k] >= 0 && ids[k] < sk)
+            if (ids[k] >= 0 && ids[k] < sk) {
+                if (seen[ids[k]]) {
+                    free(seen);
+                    return -2;
+                }
                 seen[ids[k]] = 1;
+            }
         for (int n = 0; n < sk; n++)
             if (seen[n]) {
                 if (count < cap)
@@ -195,7 +205,8 @@ int oracle_attend_keys(const double *q, const oracle_cache *c, int b,
  *   q            bf16 bits [B][T][H][576]
  *   rows         n_rows triples (b, t, h)
  *   out          [n_rows][512] doubles, lse [n_rows] doubles
- * Returns 0, or -1 on a bad argument or page index.
+ * Returns 0, -1 on a bad argument or page index, or -2 when a row's top-k
+ * list repeats a position.
  */
 int oracle_mla_decode_rows(const uint16_t *q, int B, int T, int H,
                            const void *kv, int kv_format, int num_pages,
@@ -222,6 +233,11 @@ int oracle_mla_decode_rows(const uint16_t *q, int B, int T, int H,
         int32_t *keys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1));
         int nk = oracle_valid_keys(b, t, T, cache_seqlens, topk, topk_len,
                                    causal, keys, cap);
+        if (nk < 0) {
+            bad |= 2;
+            free(keys);
+            continue;
+        }
         double qd[ORACLE_D_QK];
         const uint16_t *qr = q + (((int64_t)b * T + t) * H + h) * ORACLE_D_QK;
         for (int d = 0; d < ORACLE_D_QK; d++)
@@ -231,7 +247,7 @@ int oracle_mla_decode_rows(const uint16_t *q, int B, int T, int H,
             bad |= 1;
         free(keys);
     }
-    return bad ? -1 : 0;
+    return (bad & 2) ? -2 : (bad ? -1 : 0);
 }
 
 /* Same, with an explicit key list instead of the mask rule (used to check

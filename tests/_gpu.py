@@ -64,13 +64,3 @@ def compare_rows(w, res, rows, oracle):
 
 def all_rows(w):
     return [(b, t, h) for b in range(w.B) for t in range(w.T) for h in range(w.H)]
-
-
-def sample_rows(w, per_batch=4, batches=None):
-    """A deterministic spread of rows: shortest, longest, first and last
-    sequences (or the given ones), heads 0, 1, H/2, H-1, every query token."""
-    sk = w.cache_seqlens
-    if batches is None:
-        batches = sorted({0, w.B - 1, int(np.argmax(sk)), int(np.argmin(sk))})
-    heads = sorted({0, 1 % w.H, w.H // 2, w.H - 1})[:per_batch]
-    return [(b, t, h) for b in batches for t in range(w.T) for h in heads]

@@ -134,3 +134,30 @@ def test_library_missing_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError):
         m.num_items(1, 64, 1)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(out_shape=(2, 1, 64, 256)), "out must be"),
+    (dict(out_shape=(2, 1, 32, 512)), "out must be"),
+    (dict(lse_shape=(2, 1, 64)), "lse must be"),
+    (dict(lse_shape=(2, 64)), "lse must be"),
+    (dict(kv_scales_shape=(8, 64, 1)), "kv_scales must be"),
+    (dict(kv_scales_shape=(4, 64, 4)), "kv_scales must be"),
+    (dict(tile_md_shape=(76, 4)), "tile_md must be"),
+    (dict(tile_md_shape=(608,)), "tile_md must be"),
+    (dict(num_splits_numel=2, n_items=2), "num_splits needs"),
+    (dict(gathered_shape=(2, 1, 7), topk=8), "gathered must be"),
+])
+def test_binding_rejects_wrong_buffer_shapes(kw, msg):
+    """The C ABI receives only pointers, so the binding checks the shapes of
+    caller-given buffers: an output, scale array, schedule or gathered record
+    of the wrong shape raises ValueError before any call (a short buffer
+    would otherwise be written past its end)."""
+    import mla_decode_attention_05_gb300 as m
+    args = dict(out_shape=(2, 1, 64, 512), lse_shape=(2, 64, 1), kv_scales_shape=(8, 64, 4),
+                tile_md_shape=(76, 8), num_splits_numel=3, n_items=2, gathered_shape=None, topk=0)
+    m.check_decode_shapes(2, 1, 64, 0, 8, **{k: v for k, v in args.items() if k != "topk"})
+    args.update(kw)
+    topk = args.pop("topk")
+    with pytest.raises(ValueError, match=msg):
+        m.check_decode_shapes(2, 1, 64, topk, 8, **args)

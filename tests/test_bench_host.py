@@ -46,3 +46,23 @@ def test_clock_summary_without_samples_inside():
     c = bench.summarise_clocks(text, base + 0.5, base + 0.6)               # nearest sample to the start
     assert c["samples"] == 1 and c["sm_mhz"] == 1980.0 and c["reasons"] == [] and not c["in_timed_region"]
     assert bench.summarise_clocks("", base, base + 1) == {"samples": 0}
+
+
+def test_l2_flush_decision_of_named_workloads():
+    """Workloads whose step touches less than twice the L2 (the tiny, paged
+    and sparse ones) are timed with the L2 flushed before every step, and
+    their `config.l2` label says so; the long ones are larger than L2."""
+    l2 = 129 * 1024 * 1024
+    flushed = {}
+    for i in range(1, 6):
+        w = W.config(i)
+        kv, _ = bench.work_of(w)
+        touched = bench.step_bytes(w, kv)
+        flushed[i] = touched < 2 * l2
+        label = bench.l2_label(touched, l2, flushed[i])
+        assert ("flushed before every timed step" in label) == flushed[i]
+        assert f"{touched / 1e6:.1f} MB touched" in label
+    assert flushed == {1: True, 2: True, 3: False, 4: True, 5: False}
+    w2 = W.config(2)
+    rows = 16 * 128
+    assert bench.step_bytes(w2, 75_497_472) == 75_497_472 + rows * (1152 + 1024 + 4)

@@ -1,8 +1,7 @@
 """GPU parity: the CUDA path through the C ABI against the float64 oracle on
-the same seeded inputs.  Small cases are compared row by row in full; the
-five named workloads run at full size in the launch configuration the bench
-uses (default worker count) and are compared on sampled rows plus
-properties that hold for every row."""
+the same seeded inputs.  Small cases and the five named workloads (at full
+size, in the launch configuration the bench uses: the default worker count)
+are compared row by row in full."""
 import zlib
 
 import numpy as np
@@ -40,20 +39,23 @@ def test_tiny_dense_full(mla, oracle_mod):
 
 
 @pytest.mark.parametrize("cfg", [2, 3, 5])
-def test_dense_configs_sampled(mla, oracle_mod, cfg):
+def test_dense_configs_every_row(mla, oracle_mod, cfg):
+    """The full-size dense workloads in the bench's launch configuration,
+    every (b, t, h) row against the oracle element by element (the oracle
+    takes about 12 s for the 8192 rows of the largest on 16 host cores)."""
     w = workloads.config(cfg)
     res = G.run(w)
-    G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
-    # any-size properties: finite LSE, O a convex combination of V rows
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
     assert np.all(np.isfinite(res["lse"]))
-    assert np.abs(res["out"]).max() <= 0.5 * 6
     _status_clean(mla)
 
 
-def test_sparse_fp8_config_sampled_and_gathered(mla, oracle_mod):
+def test_sparse_fp8_config_every_row_and_gathered(mla, oracle_mod):
+    """The full-size sparse FP8 workload: every row against the oracle and
+    every sequence's gathered-index record against the oracle's valid set."""
     w = workloads.config(4)
     res = G.run(w, record=True)
-    G.compare_rows(w, res, G.sample_rows(w, batches=[0, 7, 31]), oracle_mod)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
     for b in range(w.B):
         got = res["gathered"][b, 0]
         assert np.all(got >= -1)
@@ -140,7 +142,7 @@ def test_schedule_reused_by_consecutive_calls(mla, oracle_mod):
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
     res = dict(out=outs[0][0].float().cpu().numpy().astype(np.float64),
                lse=outs[0][1].cpu().numpy().astype(np.float64))
-    G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
 
 
 def test_more_workers_than_fit_at_once(mla, oracle_mod):
@@ -150,7 +152,7 @@ def test_more_workers_than_fit_at_once(mla, oracle_mod):
     w = make_workload("waves", 2, 1, 64, [9000, 7000], seed=22)
     res = G.run(w, num_parts=120)
     assert mla.device_status() == 0
-    G.compare_rows(w, res, G.sample_rows(w), oracle_mod)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
 
 
 def test_largest_rows_per_sequence_causal(mla, oracle_mod):

@@ -376,6 +376,27 @@ def test_valid_keys_bruteforce(oracle_mod):
             assert len(exp) == 9
 
 
+def test_repeated_topk_position_is_refused(oracle_mod):
+    """The indices of one query token are distinct cache positions (a top-k
+    selection); a list that names one position twice is outside the
+    definition, so both the valid-set query and the decode refuse it instead
+    of quietly counting it once or twice.  -1 slots may repeat freely, and a
+    position repeated in another query token's list is fine."""
+    ws = make_workload("t", 2, 2, 4, [40, 30], seed=23, topk=12, topk_pad_count=3)
+    rows = [(b, t, h) for b in range(2) for t in range(2) for h in range(4)]
+    oracle_mod.decode_rows(ws, rows)                 # distinct: accepted
+    assert (ws.topk[0, 0] == -1).sum() == 3          # -1 repeats within a list
+    ws.topk[0, 1] = ws.topk[0, 0]                    # same positions, other token
+    oracle_mod.decode_rows(ws, rows)
+    valid = ws.topk[1, 1][ws.topk[1, 1] >= 0]
+    ws.topk[1, 1, int(np.argmax(ws.topk[1, 1] >= 0)) ] = valid[-1]  # a repeat
+    with pytest.raises(ValueError, match="repeats a position"):
+        oracle_mod.valid_keys(ws, 1, 1)
+    with pytest.raises(ValueError, match="repeats a position"):
+        oracle_mod.decode_rows(ws, rows)
+    assert list(oracle_mod.valid_keys(ws, 1, 0)) == sorted(int(i) for i in ws.topk[1, 0] if i >= 0)
+
+
 def test_golden_regression(oracle_mod):
     """The oracle's result on the tiny dense workload, as recorded by
     tests/golden/make_golden.py (a regression record, not a pin)."""
