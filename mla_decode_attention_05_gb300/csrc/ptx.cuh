@@ -94,6 +94,23 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are test settings: the wait then polls without
+// suspending and reads the clock at every poll, so that it can run out
+// within microseconds (a suspended try_wait may sleep far longer).
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 // Bounded wait: gives up after `limit_ns` of wall time, or at once when
 // *abort becomes non-zero; returns false then.
 template <bool kCluster = false>
@@ -101,6 +118,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int *abort, uint64_t limit_ns) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
+  if (limit_ns < kShortWaitNs) {
+    for (;;) {
+      if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
   for (uint32_t it = 1;; ++it) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
