@@ -1100,19 +1100,25 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
     if (!warp_wait(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
     tc_fence_after();
     const float inv = ell > 0.f ? 1.f / ell : 0.f;
-    float *wrow = p.ws_o + (ri.slot * M_TILE + r) * D_V + hf * 256;
-    // 32-byte stores: each lane writes whole L2 sectors of its row
+    // Split partials are stored chunk-major, [slot][64 chunks of 8 columns]
+    // [128 rows][8 floats]: the 32 lanes of a warp (32 consecutive rows)
+    // store one chunk as 1 KB of contiguous memory.  The TMEM load of the
+    // next 32 columns is in flight while this thread stores the current ones.
+    float *wbase = p.ws_o + ((size_t)ri.slot * 64 + hf * 32) * (M_TILE * 8) + (size_t)r * 8;
+    uint32_t o[2][32];
+    tmem_ld32(lt, o[0]);
+#pragma unroll
     for (int cc = 0; cc < 8; cc++) {
-      uint32_t o[32];
-      tmem_ld32(lt + cc * 32, o);
       tmem_wait_ld();
+      if (cc + 1 < 8) tmem_ld32(lt + (cc + 1) * 32, o[(cc + 1) & 1]);
+      uint32_t(&v)[32] = o[cc & 1];
       if (!ri.ok) continue;
       if (ri.nsplit <= 1) {
         uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 16; j++) w[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+        for (int j = 0; j < 16; j++) w[j] = pack_bf16(__uint_as_float(v[2 * j]) * inv, __uint_as_float(v[2 * j + 1]) * inv);
         __nv_bfloat16 *dst = orow + cc * 32;
-        if (p.out_v8) {
+        if (p.out_v8) {  // 32-byte stores: whole L2 sectors of the row
           st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
           st_global_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
         } else {
@@ -1122,9 +1128,10 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; j++) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
+        for (int j = 0; j < 32; j++) v[j] = __float_as_uint(__uint_as_float(v[j]) * inv);
 #pragma unroll
-        for (int j = 0; j < 4; j++) st_global_v8(wrow + cc * 32 + 8 * j, *reinterpret_cast<const uint32_t(*)[8]>(&o[8 * j]));
+        for (int j = 0; j < 4; j++)
+          st_global_v8(wbase + (size_t)(cc * 4 + j) * (M_TILE * 8), *reinterpret_cast<const uint32_t(*)[8]>(&v[8 * j]));
       }
     }
     return true;
