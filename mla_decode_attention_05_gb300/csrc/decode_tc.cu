@@ -376,51 +376,52 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 
 constexpr uint32_t kGatherBar = 2;  // named barrier of the 128 gather threads
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Row pi of one tile: pool row `row` (zeros for -1) into the stage at
 // shared address st, as bf16 column blocks 0-7 (+ the RoPE block 8 when
 // rope), 128-byte swizzled (row pi of block kb at kb*8192 + pi*128, chunk j
 // at ((j ^ (pi & 7)) << 4)).
 //
-// FP8 rows: the row's first thread brings the whole row (640 bytes on rank
-// 0, the 512 e4m3 bytes on rank 1) with one bulk copy into a raw staging
-// area at the start of the stage (row pi at pi * rowbytes), completing on
-// raw_bar (issue_raw_row, one tile ahead); thousands of 16-byte requests for
-// random rows would leave the SM only a few KB in flight.  Then the row's
-// two threads dequantise it, each
-// half of its column blocks: the blocks that lie past the staging area
-// first, then, after all gather threads have read their staged bytes into
-// registers, the blocks that overwrite it.  bf16 rows are copied 16 bytes at
-// a time straight into place, the blocks shared between the two threads.
-// FP8 rows: start the copy of the slot's raw row into the stage's staging
-// area (the row's first thread; the second only arrives), completing on
-// raw_bar.  Called a tile ahead of the dequantisation.
+// FP8 rows arrive first in a raw staging area at the start of the stage (row
+// pi at pi * rowbytes; issue_raw_tile, one tile ahead).  Then the row's two
+// threads dequantise it, each half of its column blocks: the blocks that lie
+// past the staging area first, then, after all gather threads have read their
+// staged bytes into registers, the blocks that overwrite it.  bf16 rows are
+// copied 16 bytes at a time straight into place, the blocks shared between
+// the two threads.
+
 // Bytes of an FP8 cache row: 640 (e4m3 latent + bf16 RoPE), or 576 in the
 // per-tensor format (all e4m3).
 __device__ __forceinline__ uint32_t fp8_row_bytes(const DecodeParams &p) {
   return p.kv_format == MLA_KV_FP8_E4M3_TENSOR ? D_QK : FP8_ROW;
 }
 
-__device__ __forceinline__ void issue_raw_row(const Ctx &c, long long row, uint32_t st, int pi, int half, bool rope,
-                                              uint64_t *raw_bar) {
+// FP8 rows of one tile into the stage's staging area, completing on raw_bar
+// (one arrival per gather thread, made when its copies have landed).  Each
+// gather warp copies 16 rows, one row at a time with all 32 lanes: every
+// 16-byte cp.async of a warp instruction reads the same 512 contiguous bytes
+// of one row (the first 512 bytes, then the RoPE bytes on rank 0), so the
+// requests are coalesced and up to a whole tile of rows is in flight per SM.
+// (One bulk copy per row went through the copy engine one row at a time:
+// about 6 us for a tile's 64 rows.)  Lane l of the warp holds the pool row
+// of key slot (gt & 32) + l; warps of half 0 copy slots 0-15 of their 32,
+// those of half 1 slots 16-31.  A row of -1 is filled with zeros.
+__device__ __forceinline__ void issue_raw_tile(const Ctx &c, long long row, uint32_t st, int gt, bool rope,
+                                               uint64_t *raw_bar) {
   const uint32_t stride = fp8_row_bytes(*c.p);
   const uint32_t rowbytes = rope ? stride : 512;
-  const uint32_t raw = st + pi * rowbytes;
-  const uint32_t rb = smem_u32(raw_bar);
-  if (half == 0 && row >= 0) {
-    mbar_arrive_expect_tx(rb, rowbytes);
-    bulk_g2s(raw, c.p->kv + row * stride, rowbytes, rb);
-  } else {
-    if (half == 0)
-      for (uint32_t j = 0; j < rowbytes; j += 16) st_shared_v4(raw + j, make_uint4(0, 0, 0, 0));
-    mbar_arrive(rb);
+  const int lane = gt & 31, sbase = gt & 32, h = gt >> 6;
+  const bool tail = rope && (uint32_t)lane * 16 + 512 < rowbytes;
+#pragma unroll 4
+  for (int k = 0; k < 16; k++) {
+    const int j = h * 16 + k;
+    const long long rj = __shfl_sync(0xffffffffu, row, j);
+    const bool ok = rj >= 0;
+    const uint8_t *src = c.p->kv + (ok ? rj : 0) * stride + lane * 16;
+    const uint32_t dst = st + (sbase + j) * rowbytes + lane * 16;
+    cp_async16(dst, src, ok);
+    if (tail) cp_async16(dst + 512, src + 512, ok);
   }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(raw_bar)) : "memory");
 }
 
 // The four per-128 scales of an FP8 row (the one scale of a per-tensor
@@ -563,7 +564,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       if (fp8) {
         sc_cur = row_scales(p, row_cur);
         if (!claim_stage(sq)) return false;
-        issue_raw_row(c, row_cur, kv0 + (sq % 3) * stage_bytes, pi, half, c.rank == 0, &br.raw_full[sq % 3]);
+        issue_raw_tile(c, row_cur, kv0 + (sq % 3) * stage_bytes, gt, c.rank == 0, &br.raw_full[sq % 3]);
       }
     }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
@@ -598,8 +599,8 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
           const long long row_next = slot_row(p, nn, pg0);
           sc_next = row_scales(p, row_next);
           if (!claim_stage(sq + 1)) return false;
-          issue_raw_row(c, row_next, kv0 + ((sq + 1) % 3) * stage_bytes, pi, half, c.rank == 0,
-                        &br.raw_full[(sq + 1) % 3]);
+          issue_raw_tile(c, row_next, kv0 + ((sq + 1) % 3) * stage_bytes, gt, c.rank == 0,
+                         &br.raw_full[(sq + 1) % 3]);
         }
       } else if (!claim_stage(sq)) {
         return false;
