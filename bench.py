@@ -662,7 +662,7 @@ def run_query(args, world, rank, local, hbm, peak_src):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights of the layer's shapes)",
         "config": {"workload": f"query_absorb_n{N}_h{H}", "tokens": N, "H": H, "bytes": nbytes,
                    "l2": "256 MB written before every timed call (weights 92 MB would otherwise stay in L2)",
-                   "gemms": "Q_B: cuBLAS (bf16, fp32 accumulate); W_UK: this library's tcgen05 kernel",
+                   "gemms": "Q_B and W_UK: this library's tcgen05 kernels (bf16, fp32 accumulate in TMEM)",
                    "parallelism": f"weak, {world} independent replica(s)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "traffic": None, "kernel_ms": step_ms,

@@ -239,6 +239,21 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, uint3
       : "memory");
 }
 
+// 2-D tile store shared -> global (bulk group of the issuing thread); the
+// box is clipped at the tensor's edges.  Coordinates must not be negative.
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Commit this thread's bulk stores and wait until they have read their
+// shared-memory source.
+__device__ __forceinline__ void bulk_store_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -10,14 +10,10 @@
 //   S = sum x_i^2 (exact, rounded once to fp32), mean = fp32(fp32(S / 1536)
 //   + eps), r = fp32(1 / fp32(sqrt(mean))) (0 if mean == 0),
 //   xq_i = bf16(fp32(fp32(x_i * w_i) * r)).
-// Q_B is a plain bf16 GEMM with fp32 accumulation, run by cuBLAS, which this
-// file loads at the first call (dlopen) so that the rest of the library does
-// not depend on it.  W_UK and the RoPE-row copy are one tcgen05 kernel of
-// this library (wuk_kernel below).
-#include <cublas_v2.h>
+// Q_B (qb_kernel) and W_UK with the RoPE-row copy (wuk_kernel) are tcgen05
+// GEMMs of this library with fp32 accumulation in tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <dlfcn.h>
 
 #include <cstdio>
 #include <mutex>
@@ -46,6 +42,7 @@ std::mutex g_mu_enc;
 __global__ void __launch_bounds__(kWarps * 32)
     qa_norm_kernel(const __nv_bfloat16 *q_a, int ld_qa, const __nv_bfloat16 *w_qa, float eps, int N,
                    __nv_bfloat16 *xq) {
+  grid_dep_trigger();  // the Q_B kernel may start its weight loads meanwhile
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (j >= N) return;
@@ -79,6 +76,153 @@ __global__ void __launch_bounds__(kWarps * 32)
       o[k] = *reinterpret_cast<uint32_t *>(&b2);
     }
     dst[32 * c + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---- Q_B: one CTA per 128 rows of W_QB (and per block of up to 256 tokens)
+//
+// qb[n][row] = bf16(sum_k W_QB[row][k] * xq[n][k]) is computed transposed,
+// D[row][n], so that the weight rows fill the MMA's M = 128 (a decode batch
+// has too few tokens to fill M) and the tokens are its N: A = 128 rows of
+// W_QB and B = the tokens' xq rows, both K-major, arrive as 128-byte swizzled
+// TMA boxes of 64 k-values (A 128 rows = 16 KB, B ntile rows) into a ring of
+// stages; D (128 x ntile fp32) sits in TMEM.  The step streams 75.5 MB of
+// weights for 128 heads, so it is bound by HBM: two CTAs share each SM and
+// every CTA keeps its ring of about 96 KB in flight.  Thread 0 loads, thread
+// 32 issues the MMAs (4 per stage), and the four warps read D back (lane =
+// weight row), round to bf16 and write it to shared memory as [token][128
+// rows], which one TMA store puts into qb (clipped at N and H * 192).
+constexpr int kQbThreads = 128;
+constexpr uint32_t kQbABytes = 128 * 128;   // 64 k-values x 128 weight rows (bf16)
+constexpr uint32_t kQbRingBytes = 98304;    // ring budget per CTA (two CTAs per SM)
+constexpr int kQbKSteps = D_QA / 64;        // 24
+constexpr uint64_t kQbWaitNs = 2000000000ull;
+
+__host__ __device__ inline uint32_t qb_stage_bytes(int ntile) { return kQbABytes + (uint32_t)ntile * 128; }
+__host__ __device__ inline int qb_stages(int ntile) {
+  const int st = (int)(kQbRingBytes / qb_stage_bytes(ntile));
+  return st > 4 ? 4 : st;
+}
+__host__ inline uint32_t qb_smem_bytes(int ntile) {
+  return (uint32_t)qb_stages(ntile) * qb_stage_bytes(ntile) + 128 + 1024;  // + barriers, alignment slack
+}
+
+__global__ void __launch_bounds__(kQbThreads, 2)
+    qb_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
+              const __grid_constant__ CUtensorMap o_map, int ntile, unsigned int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int stages = qb_stages(ntile);
+  const uint32_t stage_bytes = qb_stage_bytes(ntile);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + stages * stage_bytes);
+  uint64_t *empty = full + stages;
+  uint64_t *done = empty + stages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128, n0 = blockIdx.y * ntile;
+  int abort_flag = 0;  // the waits below give up only on their time limit
+  __shared__ int gave_up;  // a load or MMA wait of this CTA ran out
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    gave_up = 0;
+    for (int s = 0; s < stages; s++) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init_cluster();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t ring = smem_u32(base);
+  grid_dep_trigger();  // the W_UK kernel may start its own weight loads
+  if (threadIdx.x == 0) {  // loads
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_normal();
+    // The weights do not depend on the kernel before this one (the q_a
+    // RMSNorm): the first stages' weight boxes go out before waiting for it.
+    for (int k = 0; k < stages; k++) {
+      mbar_arrive_expect_tx(smem_u32(&full[k]), stage_bytes);
+      tma_load_2d(ring + k * stage_bytes, &w_map, smem_u32(&full[k]), 64 * k, m0, pol_w);
+    }
+    grid_dep_wait();
+    for (int k = 0; k < kQbKSteps; k++) {
+      const int s = k % stages;
+      const uint32_t dst = ring + s * stage_bytes;
+      if (k >= stages) {
+        if (!mbar_wait<false>(smem_u32(&empty[s]), ((k / stages) - 1) & 1, &abort_flag, kQbWaitNs)) {
+          atomicOr(status, MLA_STATUS_WAIT_TIMEOUT);
+          gave_up = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&full[s]), stage_bytes);
+        tma_load_2d(dst, &w_map, smem_u32(&full[s]), 64 * k, m0, pol_w);
+      }
+      tma_load_2d(dst + kQbABytes, &x_map, smem_u32(&full[s]), 64 * k, n0, pol_x);
+    }
+  } else if (threadIdx.x == 32) {  // MMAs
+    const uint32_t idesc = idesc_bf16_f32(128, ntile, false, false);
+    bool ok = true;
+    for (int k = 0; k < kQbKSteps && ok; k++) {
+      const int s = k % stages;
+      ok = mbar_wait<false>(smem_u32(&full[s]), (k / stages) & 1, &abort_flag, kQbWaitNs);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a = ring + s * stage_bytes, b = a + kQbABytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++)
+        mma_ss(tmem, smem_desc_sw128(a + kk * 32, 16, 1024), smem_desc_sw128(b + kk * 32, 16, 1024), idesc,
+               (k | kk) ? 1u : 0u);
+      mma_commit(smem_u32(&empty[s]));
+    }
+    if (ok) {
+      mma_commit(smem_u32(done));
+    } else {
+      atomicOr(status, MLA_STATUS_WAIT_TIMEOUT);
+      gave_up = 1;
+      mbar_arrive(smem_u32(done));  // release the readers; they see the flag below
+    }
+  }
+  const bool ok = mbar_wait<false>(smem_u32(done), 0, &abort_flag, kQbWaitNs);
+  if (!ok && lane == 0) atomicOr(status, MLA_STATUS_WAIT_TIMEOUT);
+  tc_fence_after();
+  // D (lane = weight row r, column = token) -> bf16 [token][128] in the ring,
+  // which every MMA has finished reading
+  const int r = warp * 32 + lane;
+  for (int c = 0; c < ntile; c += 32) {
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c, v);  // warp-wide
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j++) {
+      if (c + j < ntile) {
+        const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(v[j]));
+        *reinterpret_cast<__nv_bfloat16 *>(base + (size_t)(c + j) * 256 + r * 2) = hb;
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  // did every wait of this CTA complete?
+  const bool all_ok = __syncthreads_and(ok && *(volatile int *)&gave_up == 0);
+  if (threadIdx.x == 0 && all_ok) {
+    tma_store_2d(&o_map, ring, m0, n0);
+    bulk_store_commit_wait_read();
+  }
+  if (!all_ok) {  // a wait gave up: let copies or MMAs still in flight land before the CTA exits
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -136,6 +280,7 @@ __global__ void __launch_bounds__(kWukThreads, 1)
     const uint64_t pol = policy_evict_first();
     mbar_arrive_expect_tx(smem_u32(full), 6 * kBoxBytes);
     for (int j = 0; j < 4; j++) tma_load_2d(sw + j * kBoxBytes, &w_map, smem_u32(full), col0 + 64 * j, 128 * h, pol);
+    grid_dep_wait();  // qb is written by the Q_B kernel before this one
     for (int j = 0; j < 2; j++)
       tma_load_2d(sa + j * kBoxBytes, &a_map, smem_u32(full), h * 192 + 64 * j, n0, policy_evict_normal());
     if (mbar_wait<false>(smem_u32(full), 0, &abort_flag, kWukWaitNs)) {
@@ -151,6 +296,7 @@ __global__ void __launch_bounds__(kWukThreads, 1)
       mbar_arrive(smem_u32(done));  // nothing was issued: release the waiters
     }
   }
+  grid_dep_wait();  // (every thread: the RoPE rows below read qb)
   if (n < N && col0 == 0) {  // the RoPE rows, while the loads and MMAs run
     const uint4 *src = reinterpret_cast<const uint4 *>(qb + (size_t)n * H * QB_ROWS + h * QB_ROWS + D_NOPE);
     uint4 *dst = reinterpret_cast<uint4 *>(qrow + D_V);
@@ -208,61 +354,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A 2-D bf16 tensor map [rows][cols] (row stride ld elements) with 64 x 128
-// boxes and 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t ld) {
+// A 2-D bf16 tensor map [rows][cols] (row stride ld elements) with boxes of
+// box_cols x box_rows, 128-byte swizzled (or not swizzled).
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols = 64,
+              uint32_t box_rows = 128, bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-// cuBLAS, loaded at first use (the C entry points, by name).
-using GemmExFn = cublasStatus_t (*)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void *,
-                                    const void *, cudaDataType, int, const void *, cudaDataType, int, const void *,
-                                    void *, cudaDataType, int, cublasComputeType_t, cublasGemmAlgo_t);
-using GemmSbFn = cublasStatus_t (*)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void *,
-                                    const void *, cudaDataType, int, long long, const void *, cudaDataType, int,
-                                    long long, const void *, void *, cudaDataType, int, long long, int,
-                                    cublasComputeType_t, cublasGemmAlgo_t);
-struct Cublas {
-  cublasStatus_t (*create)(cublasHandle_t *) = nullptr;
-  cublasStatus_t (*set_stream)(cublasHandle_t, cudaStream_t) = nullptr;
-  GemmExFn gemm = nullptr;
-  GemmSbFn gemm_sb = nullptr;
-  bool ok = false;
-};
-
-std::mutex g_mu;
-
-const Cublas *cublas() {
-  static Cublas cb;
-  static bool tried = false;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!tried) {
-    tried = true;
-    void *h = dlopen("libcublas.so.13", RTLD_NOW | RTLD_GLOBAL);
-    if (!h) h = dlopen("libcublas.so", RTLD_NOW | RTLD_GLOBAL);
-    if (h) {
-      cb.create = reinterpret_cast<decltype(cb.create)>(dlsym(h, "cublasCreate_v2"));
-      cb.set_stream = reinterpret_cast<decltype(cb.set_stream)>(dlsym(h, "cublasSetStream_v2"));
-      cb.gemm = reinterpret_cast<decltype(cb.gemm)>(dlsym(h, "cublasGemmEx"));
-      cb.gemm_sb = reinterpret_cast<decltype(cb.gemm_sb)>(dlsym(h, "cublasGemmStridedBatchedEx"));
-      cb.ok = cb.create && cb.set_stream && cb.gemm && cb.gemm_sb;
-    }
-  }
-  return cb.ok ? &cb : nullptr;
-}
-
-// One handle per thread and device, created on first use and kept for the
-// life of the thread.
-constexpr int kMaxDevices = 64;
-thread_local cublasHandle_t t_handle[kMaxDevices] = {};
 
 int fail(int code, const char *msg) {
   set_last_error(msg);
@@ -294,19 +399,7 @@ int mla_query_absorb(const void *q_a, int ld_qa, const void *w_qa, float eps, co
     return fail(MLA_ERR_INVALID_ARG, "q_a, w_qa, w_qb, w_uk, q must be 16-byte aligned, workspace 256-byte aligned");
   if (workspace_bytes < mla_query_absorb_workspace_bytes(N, H))
     return fail(MLA_ERR_WORKSPACE, "workspace smaller than mla_query_absorb_workspace_bytes(N, H)");
-  const Cublas *cb = cublas();
-  if (!cb) return fail(MLA_ERR_UNSUPPORTED, "cuBLAS (libcublas.so.13) could not be loaded");
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return fail(MLA_ERR_CUDA, "cudaGetDevice failed");
-  cublasHandle_t &hd = t_handle[dev];
-  if (!hd && cb->create(&hd) != CUBLAS_STATUS_SUCCESS) {
-    hd = nullptr;
-    return fail(MLA_ERR_CUDA, "cublasCreate failed");
-  }
   cudaStream_t s = (cudaStream_t)stream;
-  if (cb->set_stream(hd, s) != CUBLAS_STATUS_SUCCESS) return fail(MLA_ERR_CUDA, "cublasSetStream failed");
-
   __nv_bfloat16 *xq = static_cast<__nv_bfloat16 *>(workspace);
   __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(workspace) +
                                                          round256((size_t)N * D_QA * 2));
@@ -315,24 +408,40 @@ int mla_query_absorb(const void *q_a, int ld_qa, const void *w_qa, float eps, co
       static_cast<const __nv_bfloat16 *>(q_a), ld_qa, static_cast<const __nv_bfloat16 *>(w_qa), eps, N, xq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
-  const float one = 1.f, zero = 0.f;
-  // Q_B: qb[n][h*192 + p] = sum_k W_QB[h*192 + p][k] xq[n][k]; column-major
-  // view: qb^T (H*192 x N) = W_QB^T^T (op T of the 1536 x H*192 matrix) * xq^T
-  if (cb->gemm(hd, CUBLAS_OP_T, CUBLAS_OP_N, H * QB_ROWS, N, D_QA, &one, w_qb, CUDA_R_16BF, D_QA, xq, CUDA_R_16BF,
-               D_QA, &zero, qb, CUDA_R_16BF, H * QB_ROWS, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) !=
-      CUBLAS_STATUS_SUCCESS)
-    return fail(MLA_ERR_CUDA, "cublasGemmEx (Q_B) failed");
-  // W_UK and the RoPE rows
-  CUtensorMap w_map, a_map;
-  if (!make_map(&w_map, w_uk, D_V, (uint64_t)H * D_NOPE, D_V) ||
+  // Q_B (tokens in blocks of up to 256) and W_UK + the RoPE rows
+  const int ntile = N >= 256 ? 256 : (N + 15) / 16 * 16;
+  CUtensorMap wq_map, x_map, o_map, w_map, a_map;
+  if (!make_map(&wq_map, w_qb, D_QA, (uint64_t)H * QB_ROWS, D_QA) ||
+      !make_map(&x_map, xq, D_QA, (uint64_t)N, D_QA, 64, (uint32_t)ntile) ||
+      !make_map(&o_map, qb, (uint64_t)H * QB_ROWS, (uint64_t)N, (uint64_t)H * QB_ROWS, 128, (uint32_t)ntile, false) ||
+      !make_map(&w_map, w_uk, D_V, (uint64_t)H * D_NOPE, D_V) ||
       !make_map(&a_map, qb, (uint64_t)H * QB_ROWS, (uint64_t)N, (uint64_t)H * QB_ROWS))
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   unsigned int *st = nullptr;
   if (status_word(&st) != MLA_OK) return fail(MLA_ERR_CUDA, "device status word unavailable");
+  e = cudaFuncSetAttribute(qb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qb_smem_bytes(256));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
+  // Q_B and W_UK are programmatic dependents of the kernel before each: they
+  // set up and start their weight loads while it finishes, and read its
+  // output only after griddepcontrol.wait.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((H * QB_ROWS + 127) / 128, (N + ntile - 1) / ntile);
+  cfg.blockDim = dim3(kQbThreads);
+  cfg.dynamicSmemBytes = qb_smem_bytes(ntile);
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, qb_kernel, wq_map, x_map, o_map, ntile, st);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   e = cudaFuncSetAttribute(wuk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWukSmem);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
-  wuk_kernel<<<dim3(H, D_V / 256, (N + 127) / 128), kWukThreads, kWukSmem, s>>>(w_map, a_map, qb, qo, N, H, st);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(H, D_V / 256, (N + 127) / 128);
+  cfg.blockDim = dim3(kWukThreads);
+  cfg.dynamicSmemBytes = kWukSmem;
+  e = cudaLaunchKernelEx(&cfg, wuk_kernel, w_map, a_map, (const __nv_bfloat16 *)qb, qo, N, H, st);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   set_last_error("");
   return MLA_OK;
