@@ -22,10 +22,8 @@
  * slot // page_size, slot % page_size).
  *
  * Ownership: the caller owns every buffer.  The library allocates no device
- * memory of its own, with two exceptions: mla_query_absorb creates a cuBLAS
- * handle (which allocates cuBLAS's workspace) at its first call on each
- * thread and device, and mla_decode_noalloc keeps one fixed scratch array per
- * device.  TMA tensor maps are encoded on the host at each call and passed as
+ * memory of its own, with one exception: mla_decode_noalloc keeps one fixed
+ * scratch array per device.  TMA tensor maps are encoded on the host at each call and passed as
  * kernel parameters.  Every call is asynchronous on `stream` and never
  * synchronises the host, except mla_device_status().
  *
@@ -305,10 +303,10 @@ int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, cons
  *   qb[h][p] = bf16(sum_k w_qb[h * 192 + p][k] * xq_k)     p < 192
  *   q[n][h][l]       = bf16(sum_{p<128} qb[h][p] * w_uk[h][p][l])   l < 512
  *   q[n][h][512 + i] = qb[h][128 + i]                               i < 64
- * The sums of products accumulate in fp32 (Q_B: a cuBLAS GEMM, loaded with
- * dlopen at the first call; W_UK: this library's tcgen05 kernel); the
- * RMSNorm is exact as stated.  A wait that gives up sets
- * MLA_STATUS_WAIT_TIMEOUT in the device status word.
+ * The sums of products accumulate in fp32 in tensor memory (Q_B and W_UK
+ * are this library's tcgen05 GEMMs); the RMSNorm is exact as stated.  The
+ * three kernels are chained by programmatic dependent launch.  A wait that
+ * gives up sets MLA_STATUS_WAIT_TIMEOUT in the device status word.
  *
  *   q_a, ld_qa  device bf16 rows, q_a values at columns 0..1535, row stride
  *               ld_qa elements (>= 1536, multiple of 8; the fused row:
@@ -322,8 +320,7 @@ int mla_kv_insert(const void *kv_c, int ld_kv, const void *k_pe, int ld_pe, cons
  *               aligned: xq bf16 [N][1536] at 0, then qb bf16 [N][H * 192] at
  *               the next multiple of 256 bytes (both left there)
  * All other pointers 16-byte aligned.  Asynchronous on `stream`.  Returns
- * MLA_OK, or MLA_ERR_UNSUPPORTED when cuBLAS cannot be loaded, or another
- * negative MLA_ERR_* code.
+ * MLA_OK or a negative MLA_ERR_* code.
  */
 size_t mla_query_absorb_workspace_bytes(int N, int H);
 int mla_query_absorb(const void *q_a, int ld_qa, const void *w_qa, float eps, const void *w_qb,

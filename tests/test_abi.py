@@ -106,8 +106,8 @@ def test_kv_insert_argument_checks(L, args, code):
     (dict(ws=272), -1), (dict(ws_bytes=64), -3), (dict(N=0, q_a=0, ws=0), 0),
 ])
 def test_query_absorb_argument_checks(L, args, code):
-    """mla_query_absorb rejects each bad argument before any CUDA or cuBLAS
-    call; N = 0 is a valid empty call."""
+    """mla_query_absorb rejects each bad argument before any CUDA call; N = 0
+    is a valid empty call."""
     base = dict(q_a=256, ld=2112, w_qa=256, eps=1e-6, w_qb=256, w_uk=256, N=4, H=128, q=256, ws=512,
                 ws_bytes=1 << 30)
     base.update(args)
