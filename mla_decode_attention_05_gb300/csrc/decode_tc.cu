@@ -395,6 +395,16 @@ __device__ __forceinline__ uint32_t fp8_row_bytes(const DecodeParams &p) {
   return p.kv_format == MLA_KV_FP8_E4M3_TENSOR ? D_QK : FP8_ROW;
 }
 
+// Staged rows sit 640, 576 or 512 bytes apart, a multiple of 128 bytes of
+// bank offset, so the same 16-byte chunk of 8 consecutive rows would fall in
+// the same 4 banks (an 8-way conflict for each reading quarter-warp).  Chunk
+// c of staged row pi is therefore stored at position raw_chunk(c, pi): its
+// low bits XORed with the row within its group of 8 chunks (4 for the 64-byte
+// tail of a 576-byte row), which spreads 8 rows over all 32 banks.
+__device__ __forceinline__ uint32_t raw_chunk(int c, int pi, int tail_mask) {
+  return c < 32 ? (uint32_t)((c & ~7) | ((c ^ pi) & 7)) : (uint32_t)(32 | ((c ^ pi) & tail_mask));
+}
+
 // FP8 rows of one tile into the stage's staging area, completing on raw_bar
 // (one arrival per gather thread, made when its copies have landed).  Each
 // gather warp copies 16 rows, one row at a time with all 32 lanes: every
@@ -411,15 +421,16 @@ __device__ __forceinline__ void issue_raw_tile(const Ctx &c, long long row, uint
   const uint32_t rowbytes = rope ? stride : 512;
   const int lane = gt & 31, sbase = gt & 32, h = gt >> 6;
   const bool tail = rope && (uint32_t)lane * 16 + 512 < rowbytes;
+  const int tm = stride == FP8_ROW ? 7 : 3;
 #pragma unroll 4
   for (int k = 0; k < 16; k++) {
-    const int j = h * 16 + k;
+    const int j = h * 16 + k, pj = sbase + j;
     const long long rj = __shfl_sync(0xffffffffu, row, j);
     const bool ok = rj >= 0;
     const uint8_t *src = c.p->kv + (ok ? rj : 0) * stride + lane * 16;
-    const uint32_t dst = st + (sbase + j) * rowbytes + lane * 16;
-    cp_async16(dst, src, ok);
-    if (tail) cp_async16(dst + 512, src + 512, ok);
+    const uint32_t dst = st + pj * rowbytes;
+    cp_async16(dst + raw_chunk(lane, pj, tm) * 16, src, ok);
+    if (tail) cp_async16(dst + raw_chunk(32 + lane, pj, tm) * 16, src + 512, ok);
   }
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(raw_bar)) : "memory");
 }
@@ -452,6 +463,7 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   }
   const uint32_t rowbytes = rope ? fp8_row_bytes(p) : 512;
   const uint32_t raw = st + pi * rowbytes;
+  const int tm = fp8_row_bytes(p) == FP8_ROW ? 7 : 3;
   // A thread whose wait gives up skips the work but still meets the other
   // gather threads at the barrier below, so all 128 leave together.
   const bool landed = wait_or_abort(c, raw_bar, raw_par);
@@ -464,7 +476,7 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       uint4 lo, hi;
-      dequant16(ld_shared_v4(raw + kb * 64 + u * 16), kb < 4 ? (kb < 2 ? sc.x : sc.y) : (kb < 6 ? sc.z : sc.w), lo, hi);
+      dequant16(ld_shared_v4(raw + raw_chunk(kb * 4 + u, pi, tm) * 16), kb < 4 ? (kb < 2 ? sc.x : sc.y) : (kb < 6 ? sc.z : sc.w), lo, hi);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
@@ -473,13 +485,14 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
 #pragma unroll
       for (int u = 0; u < 4; u++) {
         uint4 lo, hi;
-        dequant16(ld_shared_v4(raw + 512 + u * 16), sc.x, lo, hi);
+        dequant16(ld_shared_v4(raw + raw_chunk(32 + u, pi, tm) * 16), sc.x, lo, hi);
         st_shared_v4(st + 8 * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
         st_shared_v4(st + 8 * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
       }
     } else {  // 64 bf16 RoPE values, copied
 #pragma unroll
-      for (int j = 0; j < 8; j++) st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + 512 + j * 16));
+      for (int j = 0; j < 8; j++)
+        st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + raw_chunk(32 + j, pi, tm) * 16));
     }
   }
   // blocks below the staging area: half 0 takes blocks [0, lo_split), half
@@ -489,7 +502,7 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
   uint4 v[12];  // e4m3 bytes of this thread's blocks below the staging area (at most 3 x 64 bytes)
 #pragma unroll
   for (int u = 0; u < 12; u++)
-    if (u < (lo1 - lo0) * 4) v[u] = ld_shared_v4(raw + lo0 * 64 + u * 16);
+    if (u < (lo1 - lo0) * 4) v[u] = ld_shared_v4(raw + raw_chunk(lo0 * 4 + u, pi, tm) * 16);
   // every staged byte below the blocks has been read (or some thread gave up)
   if (bar_red_or(kGatherBar, kGatherThreads, !landed)) return false;
 #pragma unroll
