@@ -121,6 +121,14 @@ def num_items(B: int, H: int, T: int, topk: int = 0) -> int:
     return _check(lib().mla_decode_num_items(B, H, T, topk))
 
 
+def metadata_sizes(B: int, H: int, T: int, topk: int, num_parts: int):
+    """Element counts of the two schedule arrays -> (tile_md, num_splits)."""
+    a = ctypes.c_size_t()
+    b = ctypes.c_size_t()
+    _check(lib().mla_decode_metadata_sizes(B, H, T, topk, num_parts, ctypes.byref(a), ctypes.byref(b)))
+    return int(a.value), int(b.value)
+
+
 def workspace_bytes(B: int, H: int, T: int, topk: int, num_parts: int) -> int:
     n = lib().mla_decode_workspace_bytes(B, H, T, topk, num_parts)
     if n == 0:

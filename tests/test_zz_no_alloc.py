@@ -98,8 +98,8 @@ def _scratch_need(mla, B, H, T, topk):
     to 256 bytes, plus the decode workspace (the rule the header states)."""
     parts = mla.default_num_parts()
     r256 = lambda n: (n + 255) // 256 * 256
-    return (r256(parts * 8 * 4) + r256((mla.num_items(B, H, T, topk) + 1) * 4)
-            + mla.workspace_bytes(B, H, T, topk, parts))
+    md_elems, ns_elems = mla.metadata_sizes(B, H, T, topk, parts)
+    return r256(md_elems * 4) + r256(ns_elems * 4) + mla.workspace_bytes(B, H, T, topk, parts)
 
 
 def test_noalloc_largest_request_fits_and_one_more_is_refused(mla):
