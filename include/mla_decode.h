@@ -347,6 +347,24 @@ int mla_device_status(uint32_t *status);
 int mla_profile_events(void *before, void *after);
 
 /*
+ * Selects, for later mla_decode and mla_decode_noalloc calls made on the
+ * calling thread, how QK^T is computed for requests whose items have at most
+ * 64 query rows (T * H <= 64; H <= 64 with top-k):
+ *   0 (default): as for larger items, M = 128 MMAs with the rows past the
+ *     item zero;
+ *   1: the dual GEMM of FlashMLA issue #169 ("dual gemm": a weight-stationary
+ *     M = 64 MMA that computes two halves of the reduction in the two lane
+ *     halves of tensor memory, the halves of the scores then added by the
+ *     softmax warps): half the QK MMAs per key tile.
+ * Both give the attention defined at the top of this file.  On GB300 the
+ * dual GEMM measured slower on every H = 64 workload tried (e.g. 45 -> 51 us
+ * for B = 16, H = 64, s_k = 4096): those workloads are bound by HBM or by the
+ * row gather, not by the tensor pipe, and handing the partial scores between
+ * the softmax warps lengthens each tile's path to P.  Returns MLA_OK.
+ */
+int mla_set_dual_gemm(int enable);
+
+/*
  * Test hook for the failure path: the time limit, in nanoseconds, of every
  * bounded wait inside the decode kernel of later mla_decode and
  * mla_decode_noalloc calls made on the calling thread (0 restores the

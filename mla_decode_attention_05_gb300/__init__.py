@@ -79,6 +79,7 @@ def lib():
             L.mla_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             L.mla_profile_events.argtypes = [P, P]
             L.mla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.mla_set_dual_gemm.argtypes = [ctypes.c_int]
             _lib = L
     return _lib
 
@@ -409,6 +410,13 @@ def device_status() -> int:
     v = ctypes.c_uint32()
     _check(lib().mla_device_status(ctypes.byref(v)))
     return int(v.value)
+
+
+def set_dual_gemm(enable: bool):
+    """QK of items with at most 64 query rows as the M = 64 dual GEMM
+    (weight-stationary MMAs) for later decode calls on this thread; off by
+    default (see mla_set_dual_gemm in include/mla_decode.h)."""
+    _check(lib().mla_set_dual_gemm(1 if enable else 0))
 
 
 def set_wait_limit_ns(ns: int = 0):

@@ -19,6 +19,7 @@ thread_local char g_err[512] = "";
 thread_local cudaEvent_t g_ev_before = nullptr;
 thread_local cudaEvent_t g_ev_after = nullptr;
 thread_local unsigned long long g_wait_ns = mla::kDefaultWaitNs;
+thread_local int g_dual_gemm = 0;
 
 int fail(int code, const char *fmt, ...) {
   va_list ap;
@@ -231,6 +232,8 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.scale_log2 = softmax_scale * mla::LOG2E;
   p.wait_ns = g_wait_ns;
+  // the M = 64 dual GEMM for QK, when selected and every item has at most 64 query rows
+  p.dual = (g_dual_gemm && (topk > 0 ? H : T * H) <= 64) ? 1 : 0;
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = mla::launch_decode(p, s, g_ev_before, g_ev_after);
@@ -295,6 +298,11 @@ int mla_device_status(uint32_t *status) {
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_mla_status, &zero, sizeof zero);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   *status = v;
+  return ok();
+}
+
+int mla_set_dual_gemm(int enable) {
+  g_dual_gemm = enable ? 1 : 0;
   return ok();
 }
 

@@ -53,6 +53,7 @@ struct DecodeParams {
   int out_v8;        // out is 32-byte aligned: 32-byte stores
   float scale_log2;  // softmax_scale * log2(e)
   unsigned long long wait_ns;  // limit of every bounded device wait
+  int dual;                    // every item has at most 64 query rows: QK as a dual GEMM (M = 64, .ws)
 };
 
 // Default limit of the decode kernel's bounded waits.

@@ -70,9 +70,10 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // shared memory map (byte offsets from a 1024-aligned base)
 constexpr uint32_t OFF_KV = 0;
-constexpr uint32_t OFF_LPART = kStages0 * kStage0Bytes;             // rank 0: float[2][2][128]
+constexpr uint32_t OFF_XCHG = kStages0 * kStage0Bytes;              // rank 0, dual GEMM: S_b hand-over (8 KB)
 constexpr uint32_t OFF_RCV_P = kStages1 * kStage1Bytes;             // rank 1: 196608
 constexpr uint32_t OFF_BARS = OFF_RCV_P + 2 * kPBytes;              // 229376
+constexpr uint32_t kXchgBytes = 64 * 32 * 4;                         // 64 rows x 32 scores
 
 // TMEM columns
 constexpr uint32_t TM_Q = 0;      // rank 0: 288 columns (576 bf16 per row)
@@ -81,12 +82,27 @@ constexpr uint32_t TM_O = 0;      // rank 1: 512 columns
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
+// Dual GEMM for items of at most 64 query rows (FlashMLA issue #169, "dual
+// gemm"): the QK reduction over the 512 latent dims is split in two, blocks
+// 0, 2, 4, 6 in TMEM lanes 0-63 of Q and blocks 1, 3, 5, 7 in lanes 64-127,
+// and one weight-stationary M = 64, N = 128 MMA whose B descriptor spans a
+// block pair (block 2p in rows 0-63, block 2p + 1 in rows 64-127, 8 KB apart
+// in the K-major layout) gives the two partial score tiles S_a (lanes 0-63)
+// and S_b (lanes 64-127): 16 MMAs where M = 128 with padding took 32.  The
+// 64 RoPE dims are 4 ordinary M = 128 MMAs with Q's RoPE values in lanes
+// 0-63 and zeros in lanes 64-127.  The softmax warps of lanes 64-127 hand
+// S_b to those of lanes 0-63 through an 8 KB area of shared memory, 32
+// scores per row at a time (see dual_exchange), and write zero P rows.
+constexpr uint32_t IDESC_QK_WS = idesc_bf16_f32(64, 128, false, false);
+constexpr uint32_t TM_QROPE_DUAL = 128;           // rank 0, dual: RoPE columns of Q
+
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
 
 struct Bars {
   uint64_t kv_full[3], kv_empty[3];      // rank 0: blocks 0-4 of a K stage; rank 1: V stages
   uint64_t kv_full_b[3], kv_empty_b[3];  // rank 0: blocks 5-8 of a K stage
   uint64_t raw_full[3];                  // gather kernel: the stage's raw FP8 rows landed
+  uint64_t xfull[2], xempty[2];          // dual: S_b hand-over, scores 0-31 (0) and 32-63 (1)
   uint64_t s_full[2], s_free[2];
   uint64_t mfull[kMaskRing];
   uint64_t gfree[P_RING];   // rank 0: ring slot copied out by rank 1
@@ -104,8 +120,10 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(OFF_BARS + sizeof(Bars) <= 232448, "shared memory budget");
-static_assert(OFF_LPART + 4 * M_TILE * 4 <= OFF_BARS, "rank 0 map");
+constexpr uint32_t OFF_LPART = OFF_BARS + (sizeof(Bars) + 15) / 16 * 16;  // rank 0: float[2][2][128]
+constexpr uint32_t kSmemBytes = OFF_LPART + 4 * M_TILE * 4;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(OFF_XCHG + kXchgBytes <= OFF_BARS, "rank 0 map");
 static_assert(OFF_RCV_P % 1024 == 0, "P tiles need 1024-byte alignment");
 
 struct Meta {
@@ -214,6 +232,7 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
   const uint64_t pol = c.rank == 0 ? policy_evict_normal() : policy_evict_first();
   const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
+  const int split = p.dual ? 4 : 5;  // rank 0: first box = blocks [0, split), second = [split, 9)
   uint32_t g = 0, s = 0, ph = 1;  // stage s of tile g; parity of its previous release
   for_each_piece(p, c.part, [&](int, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
@@ -253,7 +272,7 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
           ok = wait_or_abort(c, &br.kv_empty[s], ph);
           if (ok) {
             const uint32_t bar = smem_u32(&br.kv_full[s]);
-            const uint32_t bytes = c.rank == 0 ? 5 * kBlkBytes : stage_bytes;
+            const uint32_t bytes = c.rank == 0 ? split * kBlkBytes : stage_bytes;
             mbar_arrive_expect_tx(bar, bytes);
             tma_load_4d(kv0 + s * stage_bytes, map, bar, 0, 0, 0, page < 0 ? 0 : page, pol);
           }
@@ -261,8 +280,8 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
             ok = wait_or_abort(c, &br.kv_empty_b[s], ph);
             if (ok) {
               const uint32_t bar = smem_u32(&br.kv_full_b[s]);
-              mbar_arrive_expect_tx(bar, 4 * kBlkBytes);
-              tma_load_4d(kv0 + s * stage_bytes + 5 * kBlkBytes, map_b, bar, 0, 0, 5, page < 0 ? 0 : page, pol);
+              mbar_arrive_expect_tx(bar, (9 - split) * kBlkBytes);
+              tma_load_4d(kv0 + s * stage_bytes + split * kBlkBytes, map_b, bar, 0, 0, split, page < 0 ? 0 : page, pol);
             }
           }
         }
@@ -681,6 +700,7 @@ __device__ void qk_waiter(const Ctx &c, int lane) {
   });
 }
 
+template <bool kDual>
 __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
@@ -710,10 +730,19 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
       const uint64_t kd0 = smem_desc_sw128(kv0 + s * kStage0Bytes, 16, 1024);
       const uint32_t d = tmem + TM_S + b * 64;
       if (elect_one()) {
+        if (kDual) {  // block pairs (0, 1), (2, 3)
 #pragma unroll
-        for (int i = 0; i < 20; i++) {
-          const int kb = i >> 2, kk = i & 3;
-          mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, i ? 1u : 0u);
+          for (int i = 0; i < 8; i++) {
+            const int pr = i >> 2, kk = i & 3;
+            mma_ws_ts(d, tmem + TM_Q + pr * 32 + kk * 8, kd0 + (uint64_t)(pr * 1024 + kk * 2), IDESC_QK_WS,
+                      i ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 20; i++) {
+            const int kb = i >> 2, kk = i & 3;
+            mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, i ? 1u : 0u);
+          }
         }
         mma_commit(kv_empty0 + s * 8);
       }
@@ -721,10 +750,21 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
       if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // blocks 5-8 in
       tc_fence_after();
       if (elect_one()) {
+        if (kDual) {  // block pairs (4, 5), (6, 7), then the RoPE block with zeros in lanes 64-127
 #pragma unroll
-        for (int i = 20; i < 36; i++) {
-          const int kb = i >> 2, kk = i & 3;
-          mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, 1u);
+          for (int i = 0; i < 8; i++) {
+            const int pr = 2 + (i >> 2), kk = i & 3;
+            mma_ws_ts(d, tmem + TM_Q + pr * 32 + kk * 8, kd0 + (uint64_t)(pr * 1024 + kk * 2), IDESC_QK_WS, 1u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++)
+            mma_ts(d, tmem + TM_QROPE_DUAL + kk * 8, kd0 + (uint64_t)(8 * 512 + kk * 2), IDESC_QK, 1u);
+        } else {
+#pragma unroll
+          for (int i = 20; i < 36; i++) {
+            const int kb = i >> 2, kk = i & 3;
+            mma_ts(d, tmem + TM_Q + kb * 32 + kk * 8, kd0 + (uint64_t)(kb * 512 + kk * 2), IDESC_QK, 1u);
+          }
         }
         mma_commit(kv_empty_b0 + s * 8);
         mma_commit(s_full0 + b * 8);
@@ -860,6 +900,85 @@ __device__ __noinline__ void load_q(uint32_t lane_tmem, uint32_t stage, int rr, 
   tmem_wait_st();
 }
 
+// Dual GEMM: the query row's blocks for lanes 0-63 (`upper` false: blocks
+// 0, 2, 4, 6 at columns 0, 32, 64, 96, and the RoPE block 8 at column 128)
+// or for lanes 64-127 (`upper`: blocks 1, 3, 5, 7, and zeros at 128-159);
+// hf 0 takes the first two of them and the RoPE columns, hf 1 the last two.
+__device__ __noinline__ void load_q_dual(uint32_t lane_tmem, uint32_t stage, int rr, bool ok, bool upper, int hf) {
+  for (int i = 0; i < 3; i++) {
+    if (hf == 1 && i == 2) break;
+    const int pr = 2 * hf + i;           // pair index (i < 2)
+    const bool rope = i == 2;
+    const int kb = rope ? 8 : 2 * pr + (upper ? 1 : 0);
+    const uint32_t col = rope ? TM_QROPE_DUAL : (uint32_t)pr * 32;
+    const bool live = ok && !(rope && upper);
+    uint32_t v[32];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (live)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                     : "r"(stage + kb * kBlkBytes + rr * 128 + ((j ^ (rr & 7)) << 4)));
+      v[4 * j] = x.x;
+      v[4 * j + 1] = x.y;
+      v[4 * j + 2] = x.z;
+      v[4 * j + 3] = x.w;
+    }
+    tmem_st32(lane_tmem + col, v);
+  }
+  tmem_wait_st();
+}
+
+// Dual GEMM: S_b hand-over from the softmax warps of lanes 64-127 to those of
+// lanes 0-63, in two rounds through one 8 KB area (64 rows x 32 scores, row
+// R at R * 128, 16-byte chunk j at position j ^ (R & 7) so that 8 consecutive
+// rows' chunks fall in different banks): round h carries scores 32h..32h+31,
+// written by the two warps (q = 2, 3) of half h, which hold them as `own`,
+// and added by the four warps of lanes 0-63 (to `own` for hf == h, else to
+// `oth`).  The writers of round 0 wait for the previous tile's round-1 reads,
+// those of round 1 for this tile's round-0 reads; every wait is bounded.
+__device__ __forceinline__ uint32_t xchg_addr(uint32_t xb, int R, int j) {
+  return xb + R * 128 + ((j ^ (R & 7)) << 4);
+}
+
+__device__ __forceinline__ bool dual_exchange(const Ctx &c, float (&own)[32], float (&oth)[32], int q, int hf, int R,
+                                              uint32_t g) {
+  Bars &br = *c.bars;
+  const uint32_t xb = smem_u32(c.base + OFF_XCHG);
+  const int lane = threadIdx.x & 31;
+  const uint32_t ph = g & 1;
+  for (int h = 0; h < 2; h++) {
+    if (q >= 2) {
+      if (hf != h) continue;
+      // the area is free: round 1 of the previous tile (h = 0) or round 0 of
+      // this tile (h = 1) has been read
+      const bool ok = h == 0 ? warp_wait(c, &br.xempty[1], ph ^ 1) : warp_wait(c, &br.xempty[0], ph);
+      if (!ok) return false;
+#pragma unroll
+      for (int j = 0; j < 8; j++)
+        st_shared_v4(xchg_addr(xb, R, j), make_uint4(__float_as_uint(own[4 * j]), __float_as_uint(own[4 * j + 1]),
+                                                     __float_as_uint(own[4 * j + 2]), __float_as_uint(own[4 * j + 3])));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&br.xfull[h]));
+    } else {
+      if (!warp_wait(c, &br.xfull[h], ph)) return false;
+      float(&dst)[32] = hf == h ? own : oth;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const uint4 a = ld_shared_v4(xchg_addr(xb, R, j));
+        dst[4 * j] += __uint_as_float(a.x);
+        dst[4 * j + 1] += __uint_as_float(a.y);
+        dst[4 * j + 2] += __uint_as_float(a.z);
+        dst[4 * j + 3] += __uint_as_float(a.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&br.xempty[h]));
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ float max32(const float (&v)[32]) {
   float mx[8];
 #pragma unroll
@@ -881,6 +1000,7 @@ __device__ __forceinline__ void mask32(float (&v)[32], uint32_t m) {
 // talking to each other; each exponentiates and writes its own 32 tokens of
 // the tile's P message and keeps its own part of the row sum.  The halves of
 // the row sum meet in shared memory at the last tile of a piece.
+template <bool kDual>
 __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
@@ -899,14 +1019,20 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       return true;
     }
     {  // the query rows, from the stage ring into TMEM
-      const uint32_t qs = sq + (r >> 6);  // rows past the item (ri.ok false) read nothing
-      if (!warp_wait(c, &br.kv_full[qs % 3], (qs / 3) & 1, ri.ok)) return false;
-      load_q(lt, kv0 + (qs % 3) * kStage0Bytes, r & 63, ri.ok, hf ? 5 : 0, hf ? 9 : 5);
+      // (dual: lanes 64-127 hold rows 0-63 too, in the item's single stage)
+      const int qr = kDual ? (r & 63) : r;
+      const bool qok = qr < it.rows;  // rows past the item read nothing
+      const uint32_t qs = sq + (qr >> 6);
+      if (!warp_wait(c, &br.kv_full[qs % 3], (qs / 3) & 1, qok)) return false;
+      if (kDual)
+        load_q_dual(lt, kv0 + (qs % 3) * kStage0Bytes, qr & 63, qok, q >= 2, hf);
+      else
+        load_q(lt, kv0 + (qs % 3) * kStage0Bytes, r & 63, qok, hf ? 5 : 0, hf ? 9 : 5);
       sq += q_stages(it) + (t1 - t0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&br.q_ready));
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&br.q_ready));
     const int sk = clamp_seqlen(p.seqlens[it.b], p.status);
     const int my_len = (p.topk_len > 0) ? 0x7fffffff : row_kv_len(sk, p.T, ri.t, p.causal);
     float m_ref = -INFINITY;  // reference max, raw score units
@@ -932,6 +1058,13 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&br.s_free[b]));
+      if (kDual) {  // S = S_a (lanes 0-63) + S_b (lanes 64-127)
+        if (!dual_exchange(c, own, oth, q, hf, r & 63, g)) return false;
+        if (q >= 2) {  // lanes 64-127 hold no row of their own: a fully masked row, P = 0
+          mlo = 0u;
+          mhi = 0u;
+        }
+      }
       // 2. mask (skipped for fully valid tiles) and tile max (raw units; the
       //    scale is positive)
       mask32(own, hf ? mhi : mlo);
@@ -1154,7 +1287,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
 
 // ---- kernel ---------------------------------------------------------------------
 
-template <bool kGather>
+template <bool kGather, bool kDual>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap kb_map,
                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap q_map,
@@ -1193,6 +1326,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
       mbar_init(smem_u32(&br.o_done[b]), 1);
     }
     mbar_init(smem_u32(&br.q_ready), kSoftmaxWarps);
+    for (int h = 0; h < 2; h++) {
+      mbar_init(smem_u32(&br.xfull[h]), 2);   // the two writer warps of the round
+      mbar_init(smem_u32(&br.xempty[h]), 4);  // the four reader warps
+    }
     for (int q = 0; q < 4; q++)
       for (int b = 0; b < 2; b++) mbar_init(smem_u32(&br.lsum[q][b]), 2);
     br.abort = 0;
@@ -1221,7 +1358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     producer_tma(c, rank == 0 ? &k_map : &v_map, &kb_map, &q_map, lane);
   }
   if (warp == 1) {
-    if (rank == 0) mma_qk(c, tmem);
+    if (rank == 0) mma_qk<kDual>(c, tmem);
     else mma_pv(c, tmem);
   }
   if (warp == waiter_warp(kGather)) {
@@ -1230,7 +1367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   }
   if (warp == 2 && lane == 0 && rank == 0) p_publisher(c);
   if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
-    if (rank == 0) softmax_role(c, tmem, warp, lane);
+    if (rank == 0) softmax_role<kDual>(c, tmem, warp, lane);
     else epilogue_role(c, tmem, warp, lane);
   }
 
@@ -1282,7 +1419,8 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
     // 5-8 of a page (K, rank 0) or blocks 0-7 (V, rank 1), 128-byte swizzle.
     cuuint64_t dims[4] = {64, (cuuint64_t)PAGE, 9, (cuuint64_t)p.num_pages};
     cuuint64_t strides[3] = {(cuuint64_t)D_QK * 2, 128, (cuuint64_t)D_QK * 2 * PAGE};
-    const cuuint32_t nblk[3] = {5, 4, 8};  // K blocks 0-4, K blocks 5-8, V
+    // K blocks [0, split) and [split, 9) (split = 4 for the dual GEMM, else 5), V
+    const cuuint32_t nblk[3] = {p.dual ? 4u : 5u, p.dual ? 5u : 4u, 8u};
     for (int m = 0; m < 3; m++) {
       cuuint32_t box[4] = {64, (cuuint32_t)PAGE, nblk[m], 1};
       CUresult r = fn(&maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint8_t *>(p.kv), dims, strides,
@@ -1303,8 +1441,9 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  const size_t smem = OFF_BARS + sizeof(Bars);
-  auto kern = gather ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  const size_t smem = kSmemBytes;
+  auto kern = gather ? (p.dual ? decode_tc_kernel<true, true> : decode_tc_kernel<true, false>)
+                     : (p.dual ? decode_tc_kernel<false, true> : decode_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ev_before) cudaEventRecord(ev_before, stream);

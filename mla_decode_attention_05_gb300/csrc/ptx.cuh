@@ -306,6 +306,21 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, u
       : "memory");
 }
 
+// Weight-stationary form with M = 64 and A from TMEM: lanes 0-63 of D get
+// A lanes 0-63 times B columns 0..N/2-1 and lanes 64-127 get A lanes 64-127
+// times B columns N/2..N-1, in N/2 columns (measured on sm_103a).  With the
+// two halves of a reduction in the two lane halves of A and the matching
+// halves of B, one MMA does the work of two M = 64 products.
+__device__ __forceinline__ void mma_ws_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {

@@ -230,3 +230,43 @@ def test_output_only_16_byte_aligned(mla, oracle_mod):
     assert torch.all(buf[:8] == 7.0), "wrote before the output"
     res = dict(out=o.float().cpu().numpy().astype(np.float64), lse=lse.cpu().numpy().astype(np.float64))
     G.compare_rows(w, res, G.all_rows(w), oracle_mod)
+
+
+# --- the M = 64 dual GEMM for QK (selected per thread) ----------------------------
+
+DUAL_CASES = [c for c in SMALL if (c.get("topk") and c["H"] <= 64) or (not c.get("topk") and c["T"] * c["H"] <= 64)]
+
+
+@pytest.fixture
+def dual_gemm(mla):
+    mla.set_dual_gemm(True)
+    yield
+    mla.set_dual_gemm(False)
+
+
+@pytest.mark.parametrize("case", DUAL_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items() if k != "seqlens"))
+@pytest.mark.parametrize("parts", [None, 37])
+def test_dual_gemm_small_every_row(mla, oracle_mod, dual_gemm, case, parts):
+    """Items of at most 64 rows with QK as the dual GEMM: every row against
+    the oracle (dense, causal, FP8, top-k, H = 1, 3, 16, 32, 64)."""
+    c = dict(case)
+    B, T, H, sl = c.pop("B"), c.pop("T"), c.pop("H"), c.pop("seqlens")
+    w = make_workload("small", B, T, H, sl, seed=zlib.crc32(repr(case).encode()) % 1000, **c)
+    res = G.run(w, num_parts=parts, record=True)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
+    if w.topk is not None:
+        for b in range(B):
+            for t in range(T):
+                got = res["gathered"][b, t]
+                assert np.array_equal(np.sort(got[got >= 0]), oracle_mod.valid_keys(w, b, t))
+    _status_clean(mla)
+
+
+@pytest.mark.parametrize("cfg", [1, 4])
+def test_dual_gemm_h64_workloads_every_row(mla, oracle_mod, dual_gemm, cfg):
+    """The two H = 64, T = 1 workloads (tiny dense, sparse FP8) at full size
+    with the dual GEMM, every row against the oracle."""
+    w = workloads.config(cfg)
+    res = G.run(w, record=True)
+    G.compare_rows(w, res, G.all_rows(w), oracle_mod)
+    _status_clean(mla)
