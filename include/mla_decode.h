@@ -114,8 +114,11 @@ int mla_decode_metadata_sizes(int B, int H, int T, int topk, int num_parts,
  *   num_splits     device int32 [num_items + 1], written
  *
  * Rule (identical on host and device; one 64-key tile per cache page):
- * items are M tiles of up to 128 query rows (row = t*H + h) per sequence, or
- * one query token per item with top-k; item i has n_i key tiles (ceil(s_k/64);
+ * items are M tiles of up to 128 query rows (row = t*H + h) per sequence,
+ * item mt * B + b for M tile mt of sequence b (m-tile-major: the workers that
+ * hold the same tile range of a sequence's M tiles then run at the same time
+ * and share its pages through L2), or one query token per item with top-k
+ * (item b * T + t); item i has n_i key tiles (ceil(s_k/64);
  * causal: ceil(min(s_k, s_k - T + t_last + 1)/64); top-k: ceil(topk/64)) and
  * costs n_i + 4 on a line; the line is cut into num_parts equal segments of
  * L = ceil(total / num_parts) and each tile belongs to the segment holding

@@ -63,8 +63,8 @@ combine_kernel(DecodeParams p) {
     row0 = (i % p.T) * p.H;
     rows = p.H;
   } else {
-    b = i / p.n_mt;
-    row0 = (i % p.n_mt) * M_TILE;
+    b = i % p.B;
+    row0 = (i / p.B) * M_TILE;
     rows = min(M_TILE, p.T * p.H - row0);
   }
   if (blockIdx.y * 32 >= rows) return;  // whole block

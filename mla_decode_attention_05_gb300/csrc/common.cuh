@@ -78,9 +78,12 @@ __device__ inline int clamp_seqlen(int sk, unsigned int *status) {
   return sk;
 }
 
-__device__ inline Item item_at(int i, const int32_t *seqlens, int H, int T,
-                               int topk, int causal, int n_mt,
-                               unsigned int *status) {
+// Item i: with top-k, query token i % T of sequence i / T; otherwise M tile
+// i / B of sequence i % B (m-tile-major: a sequence's M tiles share its
+// keys, and in this order the workers holding the same tile range of them
+// run at the same time, so each page is read from HBM once).
+__device__ inline Item item_at(int i, const int32_t *seqlens, int B, int H, int T,
+                               int topk, int causal, unsigned int *status) {
   Item it;
   if (topk > 0) {
     it.b = i / T;
@@ -91,8 +94,8 @@ __device__ inline Item item_at(int i, const int32_t *seqlens, int H, int T,
     it.ntiles = ceil_div(topk, PAGE);
     return it;
   }
-  it.b = i / n_mt;
-  int mt = i % n_mt;
+  it.b = i % B;
+  int mt = i / B;
   int sk = clamp_seqlen(seqlens[it.b], status);
   it.row0 = mt * M_TILE;
   int total = T * H;

@@ -173,7 +173,7 @@ __device__ __forceinline__ bool for_each_piece(const DecodeParams &p, int part, 
   const int32_t *md = p.tile_md + (size_t)part * MD_STRIDE;
   const int a = md[0], bt = md[1], z = md[2], et = md[3], fp = md[4], at_start = md[5];
   for (int i = a; i <= z; i++) {
-    Item it = item_at(i, p.seqlens, p.H, p.T, p.topk_len, p.causal, p.n_mt, p.status);
+    Item it = item_at(i, p.seqlens, p.B, p.H, p.T, p.topk_len, p.causal, p.status);
     int t0 = (i == a) ? bt : 0;
     int t1 = (i == z) ? et : it.ntiles;
     bool empty_owned = (it.ntiles == 0) && (i > a || at_start);

@@ -62,7 +62,7 @@ metadata_kernel(const int32_t *seqlens, int H, int T, int topk, int causal,
     int i = base + tid;
     int w = 0;
     if (i < n_items)
-      w = FIXED_COST + item_at(i, seqlens, H, T, topk, causal, n_mt, status).ntiles;
+      w = FIXED_COST + item_at(i, seqlens, n_items / (topk > 0 ? T : n_mt), H, T, topk, causal, status).ntiles;
     int incl = block_inclusive_scan(w, warp_sums);
     if (i < n_items) C[i + 1] = carry + incl;
     __syncthreads();

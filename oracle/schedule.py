@@ -12,8 +12,12 @@ Rule
 Work items.  The query rows of one sequence are packed head-fastest, row
 r = t*H + h (STAGE_D2.md "Strategy A": heads folded into M; row order token
 major).  Dense/causal: the rows of sequence b are cut into M tiles of up to
-128 rows, item = (b, m_tile).  Top-k: each query token has its own key set,
-so item = (b, t) with H rows.  Items are ordered b-major.
+128 rows, item = (b, m_tile), ordered m-tile-major (item m_tile * B + b):
+the M tiles of a sequence share its keys, and in this order the cost line
+holds all first M tiles, then all second ones, so the parts that hold the
+same tile range of a sequence's M tiles run at the same time and each page
+comes from HBM once.  Top-k: each query token has its own key set, so
+item = (b, t) with H rows, ordered b-major.
 
 Key tiles.  An item's keys are cut into 64-key tiles (one 64-token page):
   dense   ceil(s_k / 64)
@@ -51,14 +55,15 @@ M_TILE = 128
 def item_list(seqlens, H: int, T: int, topk: int = 0, causal: bool = False):
     """[(b, row_begin, row_count, n_tiles)] in schedule order."""
     items = []
-    for b, sk in enumerate(seqlens):
-        sk = int(sk)
-        if topk > 0:
+    if topk > 0:
+        for b in range(len(seqlens)):
             for t in range(T):
                 items.append((b, t * H, H, -(-topk // TILE)))
-            continue
-        rows = T * H
-        for r0 in range(0, rows, M_TILE):
+        return items
+    rows = T * H
+    for r0 in range(0, rows, M_TILE):
+        for b, sk in enumerate(seqlens):
+            sk = int(sk)
             cnt = min(M_TILE, rows - r0)
             if causal:
                 t_last = (r0 + cnt - 1) // H

@@ -84,8 +84,13 @@ def test_partition_random():
 
 
 def test_items_rows_and_tiles():
-    """M tiles of at most 128 rows, row = t*H + h; causal tiles follow the
-    last query token of the tile; top-k items are one query token each."""
+    """M tiles of at most 128 rows, row = t*H + h, ordered m-tile-major;
+    causal tiles follow the last query token of the tile; top-k items are
+    one query token each, ordered b-major."""
+    it = S.item_list([700, 300, 50], 64, 4, 0, False)
+    assert [(b, r0) for b, r0, _, _ in it] == [(0, 0), (1, 0), (2, 0), (0, 128), (1, 128), (2, 128)]
+    it = S.item_list([300, 200], 64, 2, 70, False)
+    assert [(b, r0) for b, r0, _, _ in it] == [(0, 0), (0, 64), (1, 0), (1, 64)]
     it = S.item_list([1000], 64, 4, 0, True)
     assert [(r0, c) for _, r0, c, _ in it] == [(0, 128), (128, 128)]
     assert it[0][3] == -(-(1000 - 4 + 1 + 1) // 64)
