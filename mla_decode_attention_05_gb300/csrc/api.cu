@@ -232,8 +232,10 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.scale_log2 = softmax_scale * mla::LOG2E;
   p.wait_ns = g_wait_ns;
-  // the M = 64 dual GEMM for QK, when selected and every item has at most 64 query rows
-  p.dual = (g_dual_gemm && (topk > 0 ? H : T * H) <= 64) ? 1 : 0;
+  // the M = 64 dual GEMM for QK, when selected, on the page path, when every
+  // item has at most 64 query rows (the row-gather kernel's shared memory
+  // holds its raw ring where the dual GEMM would hand over its scores)
+  p.dual = (g_dual_gemm && kv_format == MLA_KV_BF16 && topk == 0 && T * H <= 64) ? 1 : 0;
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = mla::launch_decode(p, s, g_ev_before, g_ev_after);

@@ -71,6 +71,13 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 // shared memory map (byte offsets from a 1024-aligned base)
 constexpr uint32_t OFF_KV = 0;
 constexpr uint32_t OFF_XCHG = kStages0 * kStage0Bytes;              // rank 0, dual GEMM: S_b hand-over (8 KB)
+// The row-gather kernel keeps two K / V stages and, in the memory of the
+// third, a ring of two raw slots for the FP8 rows of the next tiles.
+__host__ __device__ constexpr int ring_stages(bool gather) { return gather ? 2 : 3; }
+constexpr uint32_t OFF_RAW0 = 2 * kStage0Bytes;                     // gather, rank 0: 2 x 64 rows x 640 bytes
+constexpr uint32_t OFF_RAW1 = 2 * kStage1Bytes;                     // gather, rank 1: 2 x 64 rows x 512 bytes
+constexpr uint32_t kRawSlot0 = PAGE * FP8_ROW;
+constexpr uint32_t kRawSlot1 = PAGE * 512;
 constexpr uint32_t OFF_RCV_P = kStages1 * kStage1Bytes;             // rank 1: 196608
 constexpr uint32_t OFF_BARS = OFF_RCV_P + 2 * kPBytes;              // 229376
 constexpr uint32_t kXchgBytes = 64 * 32 * 4;                         // 64 rows x 32 scores
@@ -122,6 +129,8 @@ struct Bars {
 };
 constexpr uint32_t OFF_LPART = OFF_BARS + (sizeof(Bars) + 15) / 16 * 16;  // rank 0: float[2][2][128]
 constexpr uint32_t kSmemBytes = OFF_LPART + 4 * M_TILE * 4;
+static_assert(OFF_RAW0 + 2 * kRawSlot0 <= OFF_BARS, "gather raw ring, rank 0");
+static_assert(OFF_RAW1 + 2 * kRawSlot1 <= OFF_RCV_P, "gather raw ring, rank 1");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(OFF_XCHG + kXchgBytes <= OFF_BARS, "rank 0 map");
 static_assert(OFF_RCV_P % 1024 == 0, "P tiles need 1024-byte alignment");
@@ -400,13 +409,11 @@ constexpr uint32_t kGatherBar = 2;  // named barrier of the 128 gather threads
 // rope), 128-byte swizzled (row pi of block kb at kb*8192 + pi*128, chunk j
 // at ((j ^ (pi & 7)) << 4)).
 //
-// FP8 rows arrive first in a raw staging area at the start of the stage (row
-// pi at pi * rowbytes; issue_raw_tile, one tile ahead).  Then the row's two
-// threads dequantise it, each half of its column blocks: the blocks that lie
-// past the staging area first, then, after all gather threads have read their
-// staged bytes into registers, the blocks that overwrite it.  bf16 rows are
-// copied 16 bytes at a time straight into place, the blocks shared between
-// the two threads.
+// FP8 rows arrive first in a raw slot (row pi at pi * rowbytes;
+// issue_raw_tile, two tiles ahead) and are then dequantised into the stage
+// by the row's two threads, each half of its column blocks (fp8_row_to_stage).
+// bf16 rows are copied 16 bytes at a time straight into place, the blocks
+// shared between the two threads.
 
 // Bytes of an FP8 cache row: 640 (e4m3 latent + bf16 RoPE), or 576 in the
 // per-tensor format (all e4m3).
@@ -465,41 +472,40 @@ __device__ __forceinline__ float4 row_scales(const DecodeParams &p, long long ro
   return __ldg(reinterpret_cast<const float4 *>(p.kv_scales + row * 4));
 }
 
-__device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long long row, uint32_t st, int pi,
-                                                    int half, bool rope, uint64_t *raw_bar, uint32_t raw_par,
-                                                    float4 sc) {
-  const DecodeParams &p = *c.p;
+// A bf16 row (top-k over a bf16 cache): 16-byte cp.async straight into the
+// K layout, the blocks shared between the slot's two threads.
+__device__ __forceinline__ void bf16_row_to_stage(const DecodeParams &p, long long row, uint32_t st, int pi, int half,
+                                                  bool rope) {
   const bool ok = row >= 0;
   const int sw = pi & 7;
-  if (!fp8) {
-    const uint8_t *src = p.kv + (ok ? row : 0) * (D_QK * 2);
-    const int nb = rope ? 9 : 8;
-    for (int kb = half; kb < nb; kb += 2)
+  const uint8_t *src = p.kv + (ok ? row : 0) * (D_QK * 2);
+  const int nb = rope ? 9 : 8;
+  for (int kb = half; kb < nb; kb += 2)
 #pragma unroll
-      for (int j = 0; j < 8; j++) cp_async16(st + kb * kBlkBytes + pi * 128 + ((j ^ sw) << 4), src + kb * 128 + j * 16, ok);
-    cp_async_wait_all();
-    return true;
-  }
-  const uint32_t rowbytes = rope ? fp8_row_bytes(p) : 512;
-  const uint32_t raw = st + pi * rowbytes;
+    for (int j = 0; j < 8; j++) cp_async16(st + kb * kBlkBytes + pi * 128 + ((j ^ sw) << 4), src + kb * 128 + j * 16, ok);
+  cp_async_wait_all();
+}
+
+// An FP8 row from its raw slot (row pi at raw, chunks placed by raw_chunk)
+// into the stage as bf16 column blocks: half 0 takes latent blocks 0-3 and,
+// on rank 0, the RoPE block; half 1 takes blocks 4-7.
+__device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t raw, uint32_t st, int pi, int half,
+                                                 bool rope, float4 sc) {
   const int tm = fp8_row_bytes(p) == FP8_ROW ? 7 : 3;
-  // A thread whose wait gives up skips the work but still meets the other
-  // gather threads at the barrier below, so all 128 leave together.
-  const bool landed = wait_or_abort(c, raw_bar, raw_par);
-  // rank 0: raw rows fill bytes 0..40959, blocks 5-8 lie past them (half 0:
-  // 5, 6; half 1: 7 and the RoPE block); rank 1: bytes 0..32767, blocks 4-7
-  // lie past them (half 0: 4, 5; half 1: 6, 7)
-  const int split = rope ? 5 : 4;
-  const int hi0 = split + 2 * half, hi1 = landed ? (half ? 8 : split + 2) : hi0;
-  for (int kb = hi0; kb < hi1; kb++)
+  const int sw = pi & 7;
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const int kb = half * 4 + k;
+    const float scl = half ? (k < 2 ? sc.z : sc.w) : (k < 2 ? sc.x : sc.y);
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       uint4 lo, hi;
-      dequant16(ld_shared_v4(raw + raw_chunk(kb * 4 + u, pi, tm) * 16), kb < 4 ? (kb < 2 ? sc.x : sc.y) : (kb < 6 ? sc.z : sc.w), lo, hi);
+      dequant16(ld_shared_v4(raw + raw_chunk(kb * 4 + u, pi, tm) * 16), scl, lo, hi);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u) ^ sw) << 4), lo);
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
-  if (landed && rope && half == 1) {
+  }
+  if (rope && half == 0) {
     if (p.kv_format == MLA_KV_FP8_E4M3_TENSOR) {  // 64 e4m3 RoPE values x the scale
 #pragma unroll
       for (int u = 0; u < 4; u++) {
@@ -514,26 +520,6 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
         st_shared_v4(st + 8 * kBlkBytes + pi * 128 + ((j ^ sw) << 4), ld_shared_v4(raw + raw_chunk(32 + j, pi, tm) * 16));
     }
   }
-  // blocks below the staging area: half 0 takes blocks [0, lo_split), half
-  // 1 [lo_split, split) (rank 0: 0-2 | 3-4; rank 1: 0-1 | 2-3)
-  const int lo_split = rope ? 3 : 2;
-  const int lo0 = half ? lo_split : 0, lo1 = landed ? (half ? split : lo_split) : lo0;
-  uint4 v[12];  // e4m3 bytes of this thread's blocks below the staging area (at most 3 x 64 bytes)
-#pragma unroll
-  for (int u = 0; u < 12; u++)
-    if (u < (lo1 - lo0) * 4) v[u] = ld_shared_v4(raw + raw_chunk(lo0 * 4 + u, pi, tm) * 16);
-  // every staged byte below the blocks has been read (or some thread gave up)
-  if (bar_red_or(kGatherBar, kGatherThreads, !landed)) return false;
-#pragma unroll
-  for (int u = 0; u < 12; u++) {
-    if (u >= (lo1 - lo0) * 4) break;
-    const int kb = lo0 + (u >> 2), ch = 2 * (u & 3);
-    uint4 lo, hi;
-    dequant16(v[u], kb < 2 ? sc.x : (kb < 4 ? sc.y : sc.z), lo, hi);
-    st_shared_v4(st + kb * kBlkBytes + pi * 128 + ((ch ^ sw) << 4), lo);
-    st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((ch + 1) ^ sw) << 4), hi);
-  }
-  return true;
 }
 
 // Threads gt and gt + 64 (gt < 64) of the gather warps (0, 3, 13, 14) own
@@ -541,14 +527,25 @@ __device__ __forceinline__ bool gather_row_to_stage(const Ctx &c, bool fp8, long
 // of it, dequantised to bf16, into row pi of the column blocks of the stage
 // (9 blocks on rank 0, 8 on rank 1).  On rank 0 the first thread of the slot
 // also publishes the tile's validity mask and the gathered-index record.
+//
+// FP8 rows go through a ring of two raw slots of their own (in the memory of
+// the kernel's third stage): the rows of tile t + 2 are fetched into tile
+// t's slot as soon as every gather thread has read it, so a fetch has about
+// two tiles' time to land, and a K / V stage is held only from its tile's
+// dequantisation to the MMA that reads it.
 __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) {
+  constexpr uint32_t NS = ring_stages(true);
   const int pi = gt & 63, half = gt >> 6;
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format != MLA_KV_BF16;
+  const bool rope = c.rank == 0;
   const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
-  uint32_t g = 0, sq = 0;  // tiles; stages of the ring (rank 0: query stages too)
+  const uint32_t raw0 = smem_u32(c.base + (c.rank == 0 ? OFF_RAW0 : OFF_RAW1));
+  const uint32_t raw_slot = c.rank == 0 ? kRawSlot0 : kRawSlot1;
+  const uint32_t rowbytes = rope ? fp8_row_bytes(p) : 512;
+  uint32_t g = 0, sq = 0, rt = 0;  // tiles; stages of the ring (rank 0: query stages too); raw-slot uses
   for_each_piece(p, c.part, [&](int idx, const Item &it, int t0, int t1, int, bool empty) {
     if (empty) return true;
     const int t_item = (p.topk_len > 0) ? (idx % p.T) : 0;
@@ -556,9 +553,9 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
     if (c.rank == 0) {  // the query rows, by TMA (thread 0 issues, all 64 arrive)
       const int qrow = it.b * p.T * p.H + it.row0;
       for (int qh = 0; qh < q_stages(it); qh++, sq++) {
-        const uint32_t s = sq % 3;
-        bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / 3) & 1) ^ 1);
-        if (ok) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / 3) & 1) ^ 1);
+        const uint32_t s = sq % NS;
+        bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / NS) & 1) ^ 1);
+        if (ok) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / NS) & 1) ^ 1);
         if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;  // all gather threads give up together
         const uint32_t bar = smem_u32(&br.kv_full[s]);
         if (gt == 0) {
@@ -568,7 +565,6 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
           mbar_arrive(bar);
         }
         mbar_arrive(smem_u32(&br.kv_full_b[s]));
-        mbar_arrive(smem_u32(&br.raw_full[s]));  // keeps the raw barrier's phase in step with the stage
       }
     }
     // row pipeline (see slot_id): n0 / pg0 and n1 / pg1 = key and
@@ -580,27 +576,25 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
     int n1 = t0 + 1 < t1 ? slot_key(p, slot_id(p, it, t_item, t0 + 1, pi), sk) : -1;
     int pg1 = slot_page(p, it.b, n1);
     int id2 = t0 + 2 < t1 ? slot_id(p, it, t_item, t0 + 2, pi) : -2;
-    // FP8 rows: the raw copies of a tile are issued one tile ahead, into
-    // the tile's own stage once it is free
     auto claim_stage = [&](uint32_t q) -> bool {  // stage of sequence number q is free (all threads agree)
-      const uint32_t ss = q % 3;
-      bool ok = wait_or_abort(c, &br.kv_empty[ss], ((q / 3) & 1) ^ 1);
-      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[ss], ((q / 3) & 1) ^ 1);
+      const uint32_t ss = q % NS;
+      bool ok = wait_or_abort(c, &br.kv_empty[ss], ((q / NS) & 1) ^ 1);
+      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[ss], ((q / NS) & 1) ^ 1);
       return !bar_red_or(kGatherBar, kGatherThreads, !ok);
     };
-    long long row_cur = -1;
-    float4 sc_cur = make_float4(0, 0, 0, 0);
-    if (t0 < t1) {
-      int n = n0;
-      row_cur = slot_row(p, n, pg0);
-      if (fp8) {
-        sc_cur = row_scales(p, row_cur);
-        if (!claim_stage(sq)) return false;
-        issue_raw_tile(c, row_cur, kv0 + (sq % 3) * stage_bytes, gt, c.rank == 0, &br.raw_full[sq % 3]);
+    // FP8: the raw rows and scales of the piece's first two tiles
+    float4 sc0 = make_float4(0, 0, 0, 0), sc1 = make_float4(0, 0, 0, 0);
+    if (fp8) {
+      for (int k = 0; k < 2 && t0 + k < t1; k++) {
+        int n = k ? n1 : n0;
+        const long long r = slot_row(p, n, k ? pg1 : pg0);
+        if (k) sc1 = row_scales(p, r);
+        else sc0 = row_scales(p, r);
+        issue_raw_tile(c, r, raw0 + ((rt + k) % 2) * raw_slot, gt, rope, &br.raw_full[(rt + k) % 2]);
       }
     }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
-      const uint32_t s = sq % 3;
+      const uint32_t s = sq % NS;
       const int id3 = tile + 3 < t1 ? slot_id(p, it, t_item, tile + 3, pi) : -2;
       const int n2 = slot_key(p, id2, sk);
       const int pg2 = slot_page(p, it.b, n2);
@@ -608,7 +602,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       const long long row = slot_row(p, n, pg0);
       n0 = n1;
       pg0 = pg1;
-      n1 = n2;
+      n1 = n2;  // n1 / pg1: tile + 2 from here on
       pg1 = pg2;
       id2 = id3;
       if (c.rank == 0 && half == 0) {
@@ -622,25 +616,26 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      float4 sc_next = make_float4(0, 0, 0, 0);
+      if (!claim_stage(sq)) return false;
       if (fp8) {
-        // the next tile's raw rows and scales start landing while this one
-        // is dequantised
-        if (tile + 1 < t1) {
-          int nn = n0;
-          const long long row_next = slot_row(p, nn, pg0);
-          sc_next = row_scales(p, row_next);
-          if (!claim_stage(sq + 1)) return false;
-          issue_raw_tile(c, row_next, kv0 + ((sq + 1) % 3) * stage_bytes, gt, c.rank == 0,
-                         &br.raw_full[(sq + 1) % 3]);
+        const uint32_t slot = rt % 2;
+        const uint32_t rs = raw0 + slot * raw_slot;
+        // A thread whose wait gives up skips the work but still meets the
+        // other gather threads at the barrier below, so all 128 leave together.
+        const bool landed = wait_or_abort(c, &br.raw_full[slot], (rt / 2) & 1);
+        if (landed) fp8_row_to_stage(p, rs + pi * rowbytes, kv0 + s * stage_bytes, pi, half, rope, sc0);
+        if (bar_red_or(kGatherBar, kGatherThreads, !landed)) return false;  // the slot has been read
+        sc0 = sc1;
+        if (tile + 2 < t1) {  // the slot takes the rows of tile + 2
+          int nn = n1;
+          const long long r2 = slot_row(p, nn, pg1);
+          sc1 = row_scales(p, r2);
+          issue_raw_tile(c, r2, rs, gt, rope, &br.raw_full[slot]);
         }
-      } else if (!claim_stage(sq)) {
-        return false;
+        rt++;
+      } else {
+        bf16_row_to_stage(p, row, kv0 + s * stage_bytes, pi, half, rope);
       }
-      bool ok = gather_row_to_stage(c, fp8, row, kv0 + s * stage_bytes, pi, half, c.rank == 0, &br.raw_full[s],
-                                    (sq / 3) & 1, sc_cur);
-      sc_cur = sc_next;
-      if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
       if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
@@ -676,7 +671,9 @@ __device__ __forceinline__ bool waiter_meet(bool ok) {
 // softmax of g.  The waiter meets the MMA warp once per piece (Q is in
 // TMEM) and once per tile (stage full and S[g&1] free).
 
+template <bool kGather>
 __device__ void qk_waiter(const Ctx &c, int lane) {
+  constexpr uint32_t NS = ring_stages(kGather);
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   uint32_t g = 0, qn = 0, sq = 0;  // tiles, pieces, ring stages
@@ -690,18 +687,19 @@ __device__ void qk_waiter(const Ctx &c, int lane) {
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
       if (lane == 0) {
         ok = wait_or_abort(c, &br.s_free[g & 1], ((g >> 1) & 1) ^ 1);
-        if (ok) ok = wait_or_abort(c, &br.kv_full[sq % 3], (sq / 3) & 1);
+        if (ok) ok = wait_or_abort(c, &br.kv_full[sq % NS], (sq / NS) & 1);
       }
       if (waiter_meet(ok)) return false;  // blocks 0-4 of the stage, S free
-      if (lane == 0) ok = wait_or_abort(c, &br.kv_full_b[sq % 3], (sq / 3) & 1);
+      if (lane == 0) ok = wait_or_abort(c, &br.kv_full_b[sq % NS], (sq / NS) & 1);
       if (waiter_meet(ok)) return false;  // blocks 5-8
     }
     return true;
   });
 }
 
-template <bool kDual>
+template <bool kGather, bool kDual>
 __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
+  constexpr uint32_t NS = ring_stages(kGather);
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
@@ -716,13 +714,13 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
     // (the commit arrives once the MMAs issued so far are done)
     if (elect_one())
       for (int qh = 0; qh < q_stages(it); qh++) {
-        mma_commit(kv_empty0 + ((sq + qh) % 3) * 8);
-        mma_commit(kv_empty_b0 + ((sq + qh) % 3) * 8);
+        mma_commit(kv_empty0 + ((sq + qh) % NS) * 8);
+        mma_commit(kv_empty_b0 + ((sq + qh) % NS) * 8);
       }
     __syncwarp();
     sq += q_stages(it);
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
-      const uint32_t s = sq % 3, b = g & 1;
+      const uint32_t s = sq % NS, b = g & 1;
       if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;  // blocks 0-4 in, S free
       tc_fence_after();
       // one base descriptor per tile; block kb / step kk only move its
@@ -784,7 +782,9 @@ __device__ void mma_qk(const Ctx &c, uint32_t tmem) {
 // P is in shared memory and the epilogue warps have applied any rescale
 // (o_ready).
 
+template <bool kGather>
 __device__ void pv_waiter(const Ctx &c, int lane) {
+  constexpr uint32_t NS = ring_stages(kGather);
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   uint32_t g = 0;
@@ -794,7 +794,7 @@ __device__ void pv_waiter(const Ctx &c, int lane) {
       const uint32_t b = g & 1, u = g >> 1;
       bool ok = true;
       if (lane == 0) {
-        ok = wait_or_abort(c, &br.kv_full[g % kStages1], (g / kStages1) & 1);
+        ok = wait_or_abort(c, &br.kv_full[g % NS], (g / NS) & 1);
         if (ok) ok = wait_or_abort(c, &br.p_land[b], u & 1);
         if (ok) ok = wait_or_abort(c, &br.o_ready[b], u & 1);
       }
@@ -804,7 +804,9 @@ __device__ void pv_waiter(const Ctx &c, int lane) {
   });
 }
 
+template <bool kGather>
 __device__ void mma_pv(const Ctx &c, uint32_t tmem) {
+  constexpr uint32_t NS = ring_stages(kGather);
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
@@ -816,7 +818,7 @@ __device__ void mma_pv(const Ctx &c, uint32_t tmem) {
     if (empty) return true;
     const uint32_t gfirst = g;
     for (int tile = t0; tile < t1; tile++, g++) {
-      const uint32_t s = g % kStages1, b = g & 1;
+      const uint32_t s = g % NS, b = g & 1;
       if (bar_red_or(kMmaBar, kMmaBarThreads, false)) return false;
       tc_fence_after();
       if (elect_one()) {
@@ -1000,8 +1002,9 @@ __device__ __forceinline__ void mask32(float (&v)[32], uint32_t m) {
 // talking to each other; each exponentiates and writes its own 32 tokens of
 // the tile's P message and keeps its own part of the row sum.  The halves of
 // the row sum meet in shared memory at the last tile of a piece.
-template <bool kDual>
+template <bool kGather, bool kDual>
 __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
+  constexpr uint32_t NS = ring_stages(kGather);
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const int q = w & 3, hf = (w - 4) >> 2;
@@ -1023,11 +1026,11 @@ __device__ void softmax_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       const int qr = kDual ? (r & 63) : r;
       const bool qok = qr < it.rows;  // rows past the item read nothing
       const uint32_t qs = sq + (qr >> 6);
-      if (!warp_wait(c, &br.kv_full[qs % 3], (qs / 3) & 1, qok)) return false;
+      if (!warp_wait(c, &br.kv_full[qs % NS], (qs / NS) & 1, qok)) return false;
       if (kDual)
-        load_q_dual(lt, kv0 + (qs % 3) * kStage0Bytes, qr & 63, qok, q >= 2, hf);
+        load_q_dual(lt, kv0 + (qs % NS) * kStage0Bytes, qr & 63, qok, q >= 2, hf);
       else
-        load_q(lt, kv0 + (qs % 3) * kStage0Bytes, r & 63, qok, hf ? 5 : 0, hf ? 9 : 5);
+        load_q(lt, kv0 + (qs % NS) * kStage0Bytes, r & 63, qok, hf ? 5 : 0, hf ? 9 : 5);
       sq += q_stages(it) + (t1 - t0);
       tc_fence_before();
       __syncwarp();
@@ -1358,16 +1361,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     producer_tma(c, rank == 0 ? &k_map : &v_map, &kb_map, &q_map, lane);
   }
   if (warp == 1) {
-    if (rank == 0) mma_qk<kDual>(c, tmem);
-    else mma_pv(c, tmem);
+    if (rank == 0) mma_qk<kGather, kDual>(c, tmem);
+    else mma_pv<kGather>(c, tmem);
   }
   if (warp == waiter_warp(kGather)) {
-    if (rank == 0) qk_waiter(c, lane);
-    else pv_waiter(c, lane);
+    if (rank == 0) qk_waiter<kGather>(c, lane);
+    else pv_waiter<kGather>(c, lane);
   }
   if (warp == 2 && lane == 0 && rank == 0) p_publisher(c);
   if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
-    if (rank == 0) softmax_role<kDual>(c, tmem, warp, lane);
+    if (rank == 0) softmax_role<kGather, kDual>(c, tmem, warp, lane);
     else epilogue_role(c, tmem, warp, lane);
   }
 
@@ -1442,7 +1445,9 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream, cudaEvent_
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   const size_t smem = kSmemBytes;
-  auto kern = gather ? (p.dual ? decode_tc_kernel<true, true> : decode_tc_kernel<true, false>)
+  // (the dual GEMM's exchange area lies in the gather kernel's raw ring: the
+  // host selects it for the page path only)
+  auto kern = gather ? decode_tc_kernel<true, false>
                      : (p.dual ? decode_tc_kernel<false, true> : decode_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -234,7 +234,13 @@ def test_output_only_16_byte_aligned(mla, oracle_mod):
 
 # --- the M = 64 dual GEMM for QK (selected per thread) ----------------------------
 
-DUAL_CASES = [c for c in SMALL if (c.get("topk") and c["H"] <= 64) or (not c.get("topk") and c["T"] * c["H"] <= 64)]
+# the dual GEMM serves the page path (bf16 cache, no top-k) with at most 64 rows per item
+DUAL_CASES = [c for c in SMALL if not c.get("topk") and not c.get("fp8") and not c.get("fp8_tensor")
+              and c["T"] * c["H"] <= 64] + [
+    dict(B=3, T=1, H=64, seqlens=[1000, 64, 257]),
+    dict(B=2, T=2, H=32, seqlens=[700, 129], causal=True),
+    dict(B=2, T=4, H=16, seqlens=[300, 4], causal=True),
+]
 
 
 @pytest.fixture
@@ -248,7 +254,7 @@ def dual_gemm(mla):
 @pytest.mark.parametrize("parts", [None, 37])
 def test_dual_gemm_small_every_row(mla, oracle_mod, dual_gemm, case, parts):
     """Items of at most 64 rows with QK as the dual GEMM: every row against
-    the oracle (dense, causal, FP8, top-k, H = 1, 3, 16, 32, 64)."""
+    the oracle (dense and causal, H = 1, 3, 16, 32, 64, ragged lengths)."""
     c = dict(case)
     B, T, H, sl = c.pop("B"), c.pop("T"), c.pop("H"), c.pop("seqlens")
     w = make_workload("small", B, T, H, sl, seed=zlib.crc32(repr(case).encode()) % 1000, **c)
@@ -262,10 +268,10 @@ def test_dual_gemm_small_every_row(mla, oracle_mod, dual_gemm, case, parts):
     _status_clean(mla)
 
 
-@pytest.mark.parametrize("cfg", [1, 4])
+@pytest.mark.parametrize("cfg", [1])
 def test_dual_gemm_h64_workloads_every_row(mla, oracle_mod, dual_gemm, cfg):
-    """The two H = 64, T = 1 workloads (tiny dense, sparse FP8) at full size
-    with the dual GEMM, every row against the oracle."""
+    """The tiny dense H = 64 workload with the dual GEMM, every row against
+    the oracle."""
     w = workloads.config(cfg)
     res = G.run(w, record=True)
     G.compare_rows(w, res, G.all_rows(w), oracle_mod)
