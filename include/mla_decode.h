@@ -351,8 +351,8 @@ int mla_profile_events(void *before, void *after);
 
 /*
  * Selects, for later mla_decode and mla_decode_noalloc calls made on the
- * calling thread, how QK^T is computed for requests whose items have at most
- * 64 query rows (T * H <= 64; H <= 64 with top-k):
+ * calling thread, how QK^T is computed for requests on a bf16 cache without
+ * top-k whose items have at most 64 query rows (T * H <= 64):
  *   0 (default): as for larger items, M = 128 MMAs with the rows past the
  *     item zero;
  *   1: the dual GEMM of FlashMLA issue #169 ("dual gemm": a weight-stationary
