@@ -237,8 +237,11 @@ __device__ void producer_tma(const Ctx &c, const CUtensorMap *map, const CUtenso
                              const CUtensorMap *q_map, int lane) {
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
-  // rank 1 is the last reader of each page
-  const uint64_t pol = c.rank == 0 ? policy_evict_normal() : policy_evict_first();
+  // rank 1 is the last reader of each page, unless the sequence has several
+  // M tiles: then the worker holding the same tile range of the next M tile
+  // reads the page again, at about the same time (the items are ordered
+  // m-tile-major), and it should find it in L2
+  const uint64_t pol = (c.rank == 0 || p.n_mt > 1) ? policy_evict_normal() : policy_evict_first();
   const uint32_t stage_bytes = c.rank == 0 ? kStage0Bytes : kStage1Bytes;
   const uint32_t kv0 = smem_u32(c.base + OFF_KV);
   const int split = p.dual ? 4 : 5;  // rank 0: first box = blocks [0, split), second = [split, 9)
