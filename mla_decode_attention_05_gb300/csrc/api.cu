@@ -236,6 +236,10 @@ int mla_decode(const void *q, const void *kv_cache, int kv_format,
   // item has at most 64 query rows (the row-gather kernel's shared memory
   // holds its raw ring where the dual GEMM would hand over its scores)
   p.dual = (g_dual_gemm && kv_format == MLA_KV_BF16 && topk == 0 && T * H <= 64) ? 1 : 0;
+  // the row-gather kernel, every item at most 64 query rows: rows 64-127 of
+  // the M = 128 tile are padding, so their four softmax (rank 0) and
+  // epilogue (rank 1) warps join the row gather instead
+  p.help = ((kv_format != MLA_KV_BF16 || topk > 0) && (topk > 0 ? H : T * H) <= 64) ? 1 : 0;
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = mla::launch_decode(p, s, g_ev_before, g_ev_after);

@@ -54,6 +54,8 @@ struct DecodeParams {
   float scale_log2;  // softmax_scale * log2(e)
   unsigned long long wait_ns;  // limit of every bounded device wait
   int dual;                    // every item has at most 64 query rows: QK as a dual GEMM (M = 64, .ws)
+  int help;                    // row gather, every item has at most 64 query rows: the four
+                               // softmax / epilogue warps of rows 64-127 gather instead
 };
 
 // Default limit of the decode kernel's bounded waits.

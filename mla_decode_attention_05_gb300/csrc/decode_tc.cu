@@ -336,8 +336,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Row gather: two threads per key slot (128 threads in warps 0, 3, 13, 14).
-constexpr int kGatherThreads = 128;
+// Row gather: two threads per key slot (128 threads in warps 0, 3, 13, 14),
+// or four (256 threads, also warps 6, 7, 10, 11) when every item has at most
+// 64 query rows (DecodeParams::help): a slot's threads split its column
+// blocks into NQ parts.
+__host__ __device__ constexpr int gather_threads(bool help) { return help ? 256 : 128; }
+__host__ __device__ constexpr int softmax_warps(bool help) { return help ? 4 : 8; }
 
 // Pool row of key slot pi of tile `tile` of an item: the top-k index or the
 // position, through the block table, with bounds checks; -1 for none.  It
@@ -442,18 +446,21 @@ __device__ __forceinline__ uint32_t raw_chunk(int c, int pi, int tail_mask) {
 // requests are coalesced and up to a whole tile of rows is in flight per SM.
 // (One bulk copy per row went through the copy engine one row at a time:
 // about 6 us for a tile's 64 rows.)  Lane l of the warp holds the pool row
-// of key slot (gt & 32) + l; warps of half 0 copy slots 0-15 of their 32,
-// those of half 1 slots 16-31.  A row of -1 is filled with zeros.
+// of key slot (gt & 32) + l; the NQ warps that hold the same 32 slots copy
+// 32 / NQ of them each (part h: slots h * 32 / NQ ...).  A row of -1 is
+// filled with zeros.
+template <int NQ>
 __device__ __forceinline__ void issue_raw_tile(const Ctx &c, long long row, uint32_t st, int gt, bool rope,
                                                uint64_t *raw_bar) {
+  constexpr int kRows = 32 / NQ;  // rows copied by each warp
   const uint32_t stride = fp8_row_bytes(*c.p);
   const uint32_t rowbytes = rope ? stride : 512;
   const int lane = gt & 31, sbase = gt & 32, h = gt >> 6;
   const bool tail = rope && (uint32_t)lane * 16 + 512 < rowbytes;
   const int tm = stride == FP8_ROW ? 7 : 3;
 #pragma unroll 4
-  for (int k = 0; k < 16; k++) {
-    const int j = h * 16 + k, pj = sbase + j;
+  for (int k = 0; k < kRows; k++) {
+    const int j = h * kRows + k, pj = sbase + j;
     const long long rj = __shfl_sync(0xffffffffu, row, j);
     const bool ok = rj >= 0;
     const uint8_t *src = c.p->kv + (ok ? rj : 0) * stride + lane * 16;
@@ -476,30 +483,35 @@ __device__ __forceinline__ float4 row_scales(const DecodeParams &p, long long ro
 }
 
 // A bf16 row (top-k over a bf16 cache): 16-byte cp.async straight into the
-// K layout, the blocks shared between the slot's two threads.
-__device__ __forceinline__ void bf16_row_to_stage(const DecodeParams &p, long long row, uint32_t st, int pi, int half,
+// K layout, the blocks shared among the slot's NQ threads.
+template <int NQ>
+__device__ __forceinline__ void bf16_row_to_stage(const DecodeParams &p, long long row, uint32_t st, int pi, int part,
                                                   bool rope) {
   const bool ok = row >= 0;
   const int sw = pi & 7;
   const uint8_t *src = p.kv + (ok ? row : 0) * (D_QK * 2);
   const int nb = rope ? 9 : 8;
-  for (int kb = half; kb < nb; kb += 2)
+  for (int kb = part; kb < nb; kb += NQ)
 #pragma unroll
     for (int j = 0; j < 8; j++) cp_async16(st + kb * kBlkBytes + pi * 128 + ((j ^ sw) << 4), src + kb * 128 + j * 16, ok);
   cp_async_wait_all();
 }
 
 // An FP8 row from its raw slot (row pi at raw, chunks placed by raw_chunk)
-// into the stage as bf16 column blocks: half 0 takes latent blocks 0-3 and,
-// on rank 0, the RoPE block; half 1 takes blocks 4-7.
-__device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t raw, uint32_t st, int pi, int half,
+// into the stage as bf16 column blocks: part h of NQ takes latent blocks
+// h * 8 / NQ ... (scale tile kb / 2 for block kb) and part 0, on rank 0, the
+// RoPE block too.
+template <int NQ>
+__device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t raw, uint32_t st, int pi, int part,
                                                  bool rope, float4 sc) {
+  constexpr int kBlocks = 8 / NQ;
   const int tm = fp8_row_bytes(p) == FP8_ROW ? 7 : 3;
   const int sw = pi & 7;
 #pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const int kb = half * 4 + k;
-    const float scl = half ? (k < 2 ? sc.z : sc.w) : (k < 2 ? sc.x : sc.y);
+  for (int k = 0; k < kBlocks; k++) {
+    const int kb = part * kBlocks + k;
+    const int t = kb >> 1;
+    const float scl = t == 0 ? sc.x : t == 1 ? sc.y : t == 2 ? sc.z : sc.w;
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       uint4 lo, hi;
@@ -508,7 +520,7 @@ __device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t
       st_shared_v4(st + kb * kBlkBytes + pi * 128 + (((2 * u + 1) ^ sw) << 4), hi);
     }
   }
-  if (rope && half == 0) {
+  if (rope && part == 0) {
     if (p.kv_format == MLA_KV_FP8_E4M3_TENSOR) {  // 64 e4m3 RoPE values x the scale
 #pragma unroll
       for (int u = 0; u < 4; u++) {
@@ -525,10 +537,10 @@ __device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t
   }
 }
 
-// Threads gt and gt + 64 (gt < 64) of the gather warps (0, 3, 13, 14) own
-// key slot pi = gt of every tile: both resolve the row and each writes half
-// of it, dequantised to bf16, into row pi of the column blocks of the stage
-// (9 blocks on rank 0, 8 on rank 1).  On rank 0 the first thread of the slot
+// Threads gt, gt + 64, ... (gt < 64) of the gather warps own key slot
+// pi = gt of every tile: each resolves the row and writes its part of it,
+// dequantised to bf16, into row pi of the column blocks of the stage (9
+// blocks on rank 0, 8 on rank 1).  On rank 0 the first thread of the slot
 // also publishes the tile's validity mask and the gathered-index record.
 //
 // FP8 rows go through a ring of two raw slots of their own (in the memory of
@@ -536,9 +548,11 @@ __device__ __forceinline__ void fp8_row_to_stage(const DecodeParams &p, uint32_t
 // t's slot as soon as every gather thread has read it, so a fetch has about
 // two tiles' time to land, and a K / V stage is held only from its tile's
 // dequantisation to the MMA that reads it.
+template <int NQ>
 __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) {
   constexpr uint32_t NS = ring_stages(true);
-  const int pi = gt & 63, half = gt >> 6;
+  constexpr int kThreads = 64 * NQ;
+  const int pi = gt & 63, part = gt >> 6;
   const DecodeParams &p = *c.p;
   Bars &br = *c.bars;
   const bool fp8 = p.kv_format != MLA_KV_BF16;
@@ -559,7 +573,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         const uint32_t s = sq % NS;
         bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / NS) & 1) ^ 1);
         if (ok) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / NS) & 1) ^ 1);
-        if (bar_red_or(kGatherBar, kGatherThreads, !ok)) return false;  // all gather threads give up together
+        if (bar_red_or(kGatherBar, kThreads, !ok)) return false;  // all gather threads give up together
         const uint32_t bar = smem_u32(&br.kv_full[s]);
         if (gt == 0) {
           mbar_arrive_expect_tx(bar, kStage0Bytes);
@@ -583,7 +597,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       const uint32_t ss = q % NS;
       bool ok = wait_or_abort(c, &br.kv_empty[ss], ((q / NS) & 1) ^ 1);
       if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[ss], ((q / NS) & 1) ^ 1);
-      return !bar_red_or(kGatherBar, kGatherThreads, !ok);
+      return !bar_red_or(kGatherBar, kThreads, !ok);
     };
     // FP8: the raw rows and scales of the piece's first two tiles
     float4 sc0 = make_float4(0, 0, 0, 0), sc1 = make_float4(0, 0, 0, 0);
@@ -593,7 +607,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         const long long r = slot_row(p, n, k ? pg1 : pg0);
         if (k) sc1 = row_scales(p, r);
         else sc0 = row_scales(p, r);
-        issue_raw_tile(c, r, raw0 + ((rt + k) % 2) * raw_slot, gt, rope, &br.raw_full[(rt + k) % 2]);
+        issue_raw_tile<NQ>(c, r, raw0 + ((rt + k) % 2) * raw_slot, gt, rope, &br.raw_full[(rt + k) % 2]);
       }
     }
     for (int tile = t0; tile < t1; tile++, g++, sq++) {
@@ -608,7 +622,7 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
       n1 = n2;  // n1 / pg1: tile + 2 from here on
       pg1 = pg2;
       id2 = id3;
-      if (c.rank == 0 && half == 0) {
+      if (c.rank == 0 && part == 0) {
         const uint32_t bits = __ballot_sync(0xffffffffu, row >= 0);
         const uint32_t mi = g % kMaskRing;
         if ((pi & 31) == 0) br.mask[mi][pi >> 5] = bits;
@@ -626,18 +640,18 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         // A thread whose wait gives up skips the work but still meets the
         // other gather threads at the barrier below, so all 128 leave together.
         const bool landed = wait_or_abort(c, &br.raw_full[slot], (rt / 2) & 1);
-        if (landed) fp8_row_to_stage(p, rs + pi * rowbytes, kv0 + s * stage_bytes, pi, half, rope, sc0);
-        if (bar_red_or(kGatherBar, kGatherThreads, !landed)) return false;  // the slot has been read
+        if (landed) fp8_row_to_stage<NQ>(p, rs + pi * rowbytes, kv0 + s * stage_bytes, pi, part, rope, sc0);
+        if (bar_red_or(kGatherBar, kThreads, !landed)) return false;  // the slot has been read
         sc0 = sc1;
         if (tile + 2 < t1) {  // the slot takes the rows of tile + 2
           int nn = n1;
           const long long r2 = slot_row(p, nn, pg1);
           sc1 = row_scales(p, r2);
-          issue_raw_tile(c, r2, rs, gt, rope, &br.raw_full[slot]);
+          issue_raw_tile<NQ>(c, r2, rs, gt, rope, &br.raw_full[slot]);
         }
         rt++;
       } else {
-        bf16_row_to_stage(p, row, kv0 + s * stage_bytes, pi, half, rope);
+        bf16_row_to_stage<NQ>(p, row, kv0 + s * stage_bytes, pi, part, rope);
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&br.kv_full[s]));
@@ -1176,7 +1190,12 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
   Bars &br = *c.bars;
   const int q = w & 3, hf = (w - 4) >> 2;
   const int r = q * 32 + lane;
-  const int e = (w - 4) * 32 + lane;  // 0..255: this thread's 16-byte chunks e, e+256, ...
+  // the thread's 16-byte units of the 16 KB P image (unit ch * 128 + r: key
+  // chunk ch, row r): e, e + 256, e + 512, e + 768; with `help` only the
+  // four warps of rows 0-63 run here and copy those rows' 512 units
+  const bool help = p.help;
+  const int e = help ? ((w - 4) >> 2) * 64 + (w & 3) * 32 + lane : (w - 4) * 32 + lane;
+  auto unit = [&](int k) { return help ? (2 * k + (e >> 6)) * 128 + (e & 63) : e + 256 * k; };
   const uint32_t lt = tmem + ((uint32_t)(q * 32) << 16) + TM_O + hf * 256;
   const uint32_t pbuf = smem_u32(c.base + OFF_RCV_P);
   const uint32_t gfree0 = mapa(smem_u32(&br.gfree[0]), 0);
@@ -1204,7 +1223,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       const uint4 *src = reinterpret_cast<const uint4 *>(slot);
       uint4 v[4];
 #pragma unroll
-      for (int k = 0; k < 4; k++) v[k] = __ldcg(src + e + 256 * k);
+      for (int k = 0; k < 4; k++) v[k] = __ldcg(src + unit(k));
       const Meta *m = reinterpret_cast<const Meta *>(slot + kPBytes);
       const uint4 f0 = __ldcg(reinterpret_cast<const uint4 *>(m->flags));
       const uint4 f1 = __ldcg(reinterpret_cast<const uint4 *>(m->flags) + 1);
@@ -1213,7 +1232,7 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
       // 2. shared buffer b is free once PV(g-2) is done
       if (!warp_wait(c, &br.p_empty[b], (u & 1) ^ 1)) return false;
 #pragma unroll
-      for (int k = 0; k < 4; k++) st_shared_v4(pbuf + b * kPBytes + (e + 256 * k) * 16, v[k]);
+      for (int k = 0; k < 4; k++) st_shared_v4(pbuf + b * kPBytes + unit(k) * 16, v[k]);
       // The slot goes back to rank 0 once this warp's loads are done: the P
       // chunks are consumed by the stores above, and this instruction
       // consumes the meta values, so no load is in flight at the arrive.  A
@@ -1230,7 +1249,8 @@ __device__ void epilogue_role(const Ctx &c, uint32_t tmem, int w, int lane) {
         mbar_arrive(smem_u32(&br.p_land[b]));
         mbar_arrive_remote_relaxed(gfree0 + gs * 8);
       }
-      const uint32_t fl = f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w;
+      // (with `help` only the flags of softmax warps 4, 5, 8 and 9)
+      const uint32_t fl = help ? f0.x | f0.y | f1.x | f1.y : f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w;
       if (fl != 0u) {  // rare: O *= alpha after PV(g-1), before PV(g)
         if (!warp_wait(c, &br.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
         tc_fence_after();
@@ -1309,29 +1329,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   const Ctx c{&p, base, &br, rank, (int)cluster_id_x()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // with `help`, four warps of rows 64-127 (all padding) gather instead of
+  // running the softmax (rank 0) or the O epilogue (rank 1)
+  const bool help = kGather && p.help;
+  const uint32_t n_gather = gather_threads(help), n_soft = softmax_warps(help);
   if (threadIdx.x == 0) {
     for (int s = 0; s < 3; s++) {
-      mbar_init(smem_u32(&br.kv_full[s]), kGather ? kGatherThreads : 1);
+      mbar_init(smem_u32(&br.kv_full[s]), kGather ? n_gather : 1);
       mbar_init(smem_u32(&br.kv_empty[s]), 1);
-      mbar_init(smem_u32(&br.kv_full_b[s]), kGather ? kGatherThreads : 1);
+      mbar_init(smem_u32(&br.kv_full_b[s]), kGather ? n_gather : 1);
       mbar_init(smem_u32(&br.kv_empty_b[s]), 1);
-      mbar_init(smem_u32(&br.raw_full[s]), kGatherThreads);
+      mbar_init(smem_u32(&br.raw_full[s]), n_gather);
     }
     for (int i = 0; i < kMaskRing; i++) mbar_init(smem_u32(&br.mfull[i]), kGather ? 2 : 1);
     for (int i = 0; i < P_RING; i++) {
-      mbar_init(smem_u32(&br.gfree[i]), kSoftmaxWarps);
-      mbar_init(smem_u32(&br.pwritten[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&br.gfree[i]), n_soft);
+      mbar_init(smem_u32(&br.pwritten[i]), n_soft);
       mbar_init(smem_u32(&br.p_full[i]), 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(smem_u32(&br.s_full[b]), 1);
-      mbar_init(smem_u32(&br.s_free[b]), kSoftmaxWarps);
-      mbar_init(smem_u32(&br.p_land[b]), kSoftmaxWarps);
+      mbar_init(smem_u32(&br.s_free[b]), n_soft);
+      mbar_init(smem_u32(&br.p_land[b]), n_soft);
       mbar_init(smem_u32(&br.p_empty[b]), 1);
-      mbar_init(smem_u32(&br.o_ready[b]), kSoftmaxWarps);
+      mbar_init(smem_u32(&br.o_ready[b]), n_soft);
       mbar_init(smem_u32(&br.o_done[b]), 1);
     }
-    mbar_init(smem_u32(&br.q_ready), kSoftmaxWarps);
+    mbar_init(smem_u32(&br.q_ready), n_soft);
     for (int h = 0; h < 2; h++) {
       mbar_init(smem_u32(&br.xfull[h]), 2);   // the two writer warps of the round
       mbar_init(smem_u32(&br.xempty[h]), 4);  // the four reader warps
@@ -1357,9 +1381,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
   // earlier, its blocks would only sit beside these CTAs waiting.
   grid_dep_wait();
 
+  // (warps 6, 7, 10, 11: bit 1 of the warp index set among the softmax warps)
+  const bool soft_helper = help && warp >= 4 && warp < 4 + kSoftmaxWarps && (warp & 2);
   if (kGather) {
+    int gt = -1;
     if (warp == 0 || warp == 3 || warp == 13 || warp == 14)
-      producer_gather(c, &q_map, (warp == 0 ? 0 : warp == 3 ? 32 : warp == 13 ? 64 : 96) + lane);
+      gt = (warp == 0 ? 0 : warp == 3 ? 32 : warp == 13 ? 64 : 96) + lane;
+    else if (soft_helper)
+      gt = 128 + (warp == 6 ? 0 : warp == 7 ? 32 : warp == 10 ? 64 : 96) + lane;
+    if (gt >= 0) {
+      if (help) producer_gather<4>(c, &q_map, gt);
+      else producer_gather<2>(c, &q_map, gt);
+    }
   } else if (warp == 0) {
     producer_tma(c, rank == 0 ? &k_map : &v_map, &kb_map, &q_map, lane);
   }
@@ -1372,7 +1405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of(kGather),
     else pv_waiter<kGather>(c, lane);
   }
   if (warp == 2 && lane == 0 && rank == 0) p_publisher(c);
-  if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
+  if (warp >= 4 && warp < 4 + kSoftmaxWarps && !soft_helper) {
     if (rank == 0) softmax_role<kGather, kDual>(c, tmem, warp, lane);
     else epilogue_role(c, tmem, warp, lane);
   }
