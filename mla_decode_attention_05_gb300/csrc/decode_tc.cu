@@ -641,6 +641,12 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         // other gather threads at the barrier below, so all 128 leave together.
         const bool landed = wait_or_abort(c, &br.raw_full[slot], (rt / 2) & 1);
         if (landed) fp8_row_to_stage<NQ>(p, rs + pi * rowbytes, kv0 + s * stage_bytes, pi, part, rope, sc0);
+        // this thread's part of the stage is written: it is handed to the
+        // MMA before the next raw fetch goes out, since the proxy fence waits
+        // for the thread's copies in flight
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&br.kv_full[s]));
+        if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
         if (bar_red_or(kGatherBar, kThreads, !landed)) return false;  // the slot has been read
         sc0 = sc1;
         if (tile + 2 < t1) {  // the slot takes the rows of tile + 2
@@ -652,10 +658,10 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         rt++;
       } else {
         bf16_row_to_stage<NQ>(p, row, kv0 + s * stage_bytes, pi, part, rope);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&br.kv_full[s]));
+        if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&br.kv_full[s]));
-      if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
     }
     return true;
   });
