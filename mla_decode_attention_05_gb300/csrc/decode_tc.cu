@@ -593,12 +593,6 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
     int n1 = t0 + 1 < t1 ? slot_key(p, slot_id(p, it, t_item, t0 + 1, pi), sk) : -1;
     int pg1 = slot_page(p, it.b, n1);
     int id2 = t0 + 2 < t1 ? slot_id(p, it, t_item, t0 + 2, pi) : -2;
-    auto claim_stage = [&](uint32_t q) -> bool {  // stage of sequence number q is free (all threads agree)
-      const uint32_t ss = q % NS;
-      bool ok = wait_or_abort(c, &br.kv_empty[ss], ((q / NS) & 1) ^ 1);
-      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[ss], ((q / NS) & 1) ^ 1);
-      return !bar_red_or(kGatherBar, kThreads, !ok);
-    };
     // FP8: the raw rows and scales of the piece's first two tiles
     float4 sc0 = make_float4(0, 0, 0, 0), sc1 = make_float4(0, 0, 0, 0);
     if (fp8) {
@@ -633,13 +627,16 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         __syncwarp();
         if ((pi & 31) == 0) mbar_arrive(smem_u32(&br.mfull[mi]));
       }
-      if (!claim_stage(sq)) return false;
+      // The tile's stage is free once its previous tile's MMAs are done.
+      // Each gather thread waits for that itself and writes its part; a
+      // thread whose wait gives up skips the work but still meets the other
+      // gather threads at the barrier below, so all of them leave together.
+      bool ok = wait_or_abort(c, &br.kv_empty[s], ((sq / NS) & 1) ^ 1);
+      if (ok && c.rank == 0) ok = wait_or_abort(c, &br.kv_empty_b[s], ((sq / NS) & 1) ^ 1);
       if (fp8) {
         const uint32_t slot = rt % 2;
         const uint32_t rs = raw0 + slot * raw_slot;
-        // A thread whose wait gives up skips the work but still meets the
-        // other gather threads at the barrier below, so all 128 leave together.
-        const bool landed = wait_or_abort(c, &br.raw_full[slot], (rt / 2) & 1);
+        const bool landed = ok && wait_or_abort(c, &br.raw_full[slot], (rt / 2) & 1);
         if (landed) fp8_row_to_stage<NQ>(p, rs + pi * rowbytes, kv0 + s * stage_bytes, pi, part, rope, sc0);
         // this thread's part of the stage is written: it is handed to the
         // MMA before the next raw fetch goes out, since the proxy fence waits
@@ -657,10 +654,11 @@ __device__ void producer_gather(const Ctx &c, const CUtensorMap *q_map, int gt) 
         }
         rt++;
       } else {
-        bf16_row_to_stage<NQ>(p, row, kv0 + s * stage_bytes, pi, part, rope);
+        if (ok) bf16_row_to_stage<NQ>(p, row, kv0 + s * stage_bytes, pi, part, rope);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&br.kv_full[s]));
         if (c.rank == 0) mbar_arrive(smem_u32(&br.kv_full_b[s]));
+        if (bar_red_or(kGatherBar, kThreads, !ok)) return false;
       }
     }
     return true;
