@@ -87,6 +87,8 @@ SMALL = [
     dict(B=1, T=16, H=32, seqlens=[700], causal=True),
     dict(B=2, T=4, H=64, seqlens=[900, 260], topk=130, topk_pad_count=5),
     dict(B=1, T=1, H=128, seqlens=[4160], fp8=True),
+    dict(B=2, T=4, H=16, seqlens=[300, 70], causal=True, fp8=True),   # 64 rows: padding warps gather
+    dict(B=2, T=2, H=64, seqlens=[200, 90], causal=True, fp8=True),   # 128 rows: the usual gather
 ]
 
 
