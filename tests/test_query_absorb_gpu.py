@@ -64,7 +64,7 @@ def _check(inp, strided=True):
     assert err.max() <= 0.02 * np.abs(full).max()
 
 
-@pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (37, 64), (64, 128)])
+@pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (37, 64), (64, 128), (129, 32), (300, 8)])
 def test_query_absorb_stages(N, H):
     _check(W.make_query_inputs(N, H, seed=300 + N))
 
