@@ -28,7 +28,8 @@
 //   warp 0      producer: one 4-D TMA per page (rank 0: the 9 column blocks
 //               into a 3-stage ring; rank 1: the 8 V blocks), or with warps
 //               3, 13 and 14 the row gather / FP8 dequantisation into the
-//               same layout
+//               same layout (with warps 6, 7, 10 and 11 too when every item
+//               has at most 64 query rows, since their rows are padding)
 //   warp 1      TMEM allocation and the MMA warp (one elected lane issues)
 //   warp 2      rank 0: publishes written P slots to rank 1; rank 1: idle
 //   warp 3      the MMA warp's waiter (warp 12 in the gather kernel)
