@@ -51,11 +51,13 @@ __device__ __forceinline__ void acc_add(float (&acc)[kChunks * 8], const float (
 
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(DecodeParams p) {
-  grid_dep_wait();  // the decode kernel's partials are complete
+  // the schedule was complete before any decode block began its pieces, so
+  // it is read before waiting for the decode kernel
   const int i = blockIdx.x;
   const int base = p.num_splits[i];
   const int ns = p.num_splits[i + 1] - base;
   if (ns <= 1) return;
+  grid_dep_wait();  // the decode kernel's partials are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int b, row0, rows;
   if (p.topk_len > 0) {
