@@ -194,6 +194,52 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def device_parts(local: int) -> int:
+    """Workers of the split-KV partition on this device: one cluster of two
+    CTAs per two SMs (the library's default; 76 on a 152-SM GB300 when no
+    device is visible)."""
+    try:
+        import torch
+        n = int(torch.cuda.get_device_properties(local).multi_processor_count)
+        return max(n // 2, 1)
+    except Exception:
+        return 76
+
+
+def decode_config(w, steps: int, world: int, parts: int, l2_bytes: int):
+    """The `config` object of a decode line, identical for the library's arm
+    and the reference (oracle) arm: the workload and how the timed steps
+    treat L2.  Returns (config, flush_l2)."""
+    kv_bytes, flops = work_of(w)
+    touched = step_bytes(w, kv_bytes)
+    flush = touched < 2 * l2_bytes
+    cfg = {"workload": w.name, "B": w.B, "T": w.T, "H": w.H,
+           "kv_format": "bf16" if w.kv_format == 0 else "fp8_e4m3",
+           "causal": w.causal, "topk": w.topk_len, "page_size": 64, "num_parts": parts,
+           "kv_bytes": kv_bytes, "flops": flops, "seed": w.seed,
+           "l2": l2_label(touched, l2_bytes, flush),
+           "parallelism": f"weak, {world} independent replica(s)",
+           "kernel_timing": f"decode kernel duration from a second {steps}-step loop with CUDA events around "
+                            "each decode launch"}
+    return cfg, flush
+
+
+def insert_config(N: int, num_pages: int, world: int) -> dict:
+    """The `config` of a KV-insert line (both arms)."""
+    return {"workload": f"kv_insert_fp8_tile_n{N}", "tokens": N, "page_size": 64,
+            "num_pages": num_pages, "bytes_per_token": INSERT_BYTES_PER_TOKEN,
+            "l2": f"{N * INSERT_BYTES_PER_TOKEN / 1e6:.0f} MB touched per step vs {L2_BYTES / 1e6:.0f} MB L2; no flush",
+            "parallelism": f"weak, {world} independent replica(s)"}
+
+
+def query_config(N: int, H: int, world: int) -> dict:
+    """The `config` of a query-absorption line (both arms)."""
+    return {"workload": f"query_absorb_n{N}_h{H}", "tokens": N, "H": H, "bytes": query_bytes(N, H),
+            "l2": "256 MB written before every timed call (weights 92 MB would otherwise stay in L2)",
+            "gemms": "Q_B and W_UK: this library's tcgen05 kernels (bf16, fp32 accumulate in TMEM)",
+            "parallelism": f"weak, {world} independent replica(s)"}
+
+
 def device_l2_bytes(local: int) -> int:
     """L2 size of the device (the nominal GB300 figure if torch does not
     report it)."""
@@ -541,10 +587,7 @@ def run_insert(args, world, rank, local, hbm, peak_src):
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
         "tokens_per_s": world * N / (step_ms * 1e-3),
-        "config": {"workload": f"kv_insert_fp8_tile_n{N}", "tokens": N, "page_size": 64,
-                   "num_pages": inp.num_pages, "bytes_per_token": INSERT_BYTES_PER_TOKEN,
-                   "l2": f"{N * INSERT_BYTES_PER_TOKEN / 1e6:.0f} MB touched per step vs {L2_BYTES / 1e6:.0f} MB L2; no flush",
-                   "parallelism": f"weak, {world} independent replica(s)"},
+        "config": insert_config(N, inp.num_pages, world),
         "roofline": {"bound": "hbm", "achieved": k_gbs, "peak": hbm, "unit": "GB/s", "frac": k_gbs / hbm,
                      "traffic": None, "kernel_ms": kern_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src},
@@ -660,10 +703,7 @@ def run_query(args, world, rank, local, hbm, peak_src):
         "metric": QUERY_METRIC, "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights of the layer's shapes)",
-        "config": {"workload": f"query_absorb_n{N}_h{H}", "tokens": N, "H": H, "bytes": nbytes,
-                   "l2": "256 MB written before every timed call (weights 92 MB would otherwise stay in L2)",
-                   "gemms": "Q_B and W_UK: this library's tcgen05 kernels (bf16, fp32 accumulate in TMEM)",
-                   "parallelism": f"weak, {world} independent replica(s)"},
+        "config": query_config(N, H, world),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "traffic": None, "kernel_ms": step_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src},
@@ -708,7 +748,7 @@ def main():
             print(json.dumps({"impl": "reference", "metric": QUERY_METRIC, "value": cb["value"], "unit": "GB/s",
                               "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                              "data": "synthetic", "config": {"workload": f"query_absorb_n{inp.N}_h128"},
+                              "data": "synthetic", "config": query_config(inp.N, 128, args.gpus),
                               "cpu_baseline": cb,
                               "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                                       "d2h_bytes_per_step": 0}}), flush=True)
@@ -724,7 +764,7 @@ def main():
             print(json.dumps({"impl": "reference", "metric": INSERT_METRIC, "value": cb["value"], "unit": "GB/s",
                               "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                              "data": "synthetic", "config": {"workload": f"kv_insert_fp8_tile_n{inp.N}"},
+                              "data": "synthetic", "config": insert_config(inp.N, inp.num_pages, args.gpus),
                               "cpu_baseline": cb,
                               "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                                       "d2h_bytes_per_step": 0}}), flush=True)
@@ -756,7 +796,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(per),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic",
-                "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H},
+                "config": decode_config(w, args.steps, args.gpus, device_parts(local), device_l2_bytes(local))[0],
                 "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"one sequence (all {w.T * w.H} query rows) per step, rotating over the {w.B} sequences"},
                 "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -768,8 +808,7 @@ def main():
         w = subset(w, args.batch)
     kv_bytes, flops = work_of(w)
     l2_bytes = device_l2_bytes(local)
-    touched = step_bytes(w, kv_bytes)
-    args.flush_l2 = touched < 2 * l2_bytes
+    config, args.flush_l2 = decode_config(w, args.steps, world, device_parts(local), l2_bytes)
     r = run_gpu(args, w, world, rank, local, l2_bytes)
     step_ms = max_over_ranks(r["total_ms"] / args.steps, world)
     kern_ms = statistics.mean(r["kern_ms"])
@@ -799,12 +838,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tflops": tflops, "roofline_time_us": roof_us, "frac_of_roofline": (roof_us * 1e-3) / step_ms,
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "kv_format": "bf16" if w.kv_format == 0 else "fp8_e4m3",
-                   "causal": w.causal, "topk": w.topk_len, "page_size": 64, "num_parts": r["parts"],
-                   "kv_bytes": kv_bytes, "flops": flops, "seed": w.seed,
-                   "l2": l2_label(touched, l2_bytes, args.flush_l2),
-                   "parallelism": f"weak, {world} independent replica(s)",
-                   "kernel_timing": f"decode kernel duration from a second {args.steps}-step loop with CUDA events around each decode launch"},
+        "config": config,
         "roofline": roof,
         "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

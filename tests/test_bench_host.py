@@ -66,3 +66,19 @@ def test_l2_flush_decision_of_named_workloads():
     w2 = W.config(2)
     rows = 16 * 128
     assert bench.step_bytes(w2, 75_497_472) == 75_497_472 + rows * (1152 + 1024 + 4)
+
+
+def test_reference_arm_reports_the_same_config(capsys, monkeypatch):
+    """`--impl reference` (the float64 oracle on the host) prints the same
+    `config` object as the library's arm builds for the workload, so the two
+    lines describe one benchmark."""
+    import json
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"])
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    w = W.config(3)
+    want, flush = bench.decode_config(w, 1, 1, bench.device_parts(0), bench.device_l2_bytes(0))
+    assert line["config"] == want and not flush
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["dtype"] == "f64"
